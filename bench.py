@@ -1,0 +1,511 @@
+"""Benchmark of the paged-KV decode hot path on GB300.
+
+One step = the whole hot path over one batch: pa_cache_write of the step's new
+tokens, then pa_decode over every sequence's paged context (inputs resident in
+HBM). The headline workload is the 32k-context decode (8 sequences x 32768
+tokens, 12 query / 2 KV heads, head_dim 128, bf16, 16384-block pool). The
+64-sequence decode, the Qwen2-1.5B-shaped decode and the fused speculative
+verify are measured too and reported under "per_config".
+
+Metric: achieved KV-read bandwidth (algorithmic K+V bytes of every valid token
+per step / step time, GB/s) and microseconds per call. Timing uses CUDA events
+on the launching stream, with L2 flushed (a 256 MiB write) before every timed
+step. rank 0 prints one JSON line.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+                    [--workload c4] [--no-extra]
+
+--impl reference times the fp64 CPU oracle (the only reference this method
+has) on a bounded sample of the same workload, on the host cores.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+from paged_kv_decode_pa_gb300 import accounting, inputs  # noqa: E402
+
+METRIC = "paged-decode attention: achieved KV-read HBM GB/s (% of peak), µs per call"
+L2_FLUSH_BYTES = 256 << 20
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--workload", default="c4", choices=["c2", "c3", "c4"])
+    ap.add_argument("--no-extra", action="store_true", help="skip the per_config measurements")
+    ap.add_argument("--kernel", default="auto", choices=["auto", "mma", "simt"])
+    ap.add_argument("--split-tokens", type=int, default=0)
+    ap.add_argument("--cpu-seconds", type=float, default=12.0, help="CPU baseline sample budget")
+    return ap.parse_args()
+
+
+# ---------------------------------------------------------------------------
+# distributed plumbing (one process per GPU; timing reduction only)
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        import torch
+
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend=backend)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int, device) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------------------
+# measured peaks, clocks, ncu traffic
+
+def hbm_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        if not self.path or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"]}
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        os.unlink(self.path)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "paged_kv_decode_pa_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh")):
+            h.update(open(os.path.join(csrc, name), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if it matches the current kernels."""
+    path = os.path.join(ROOT, "profiles", "decode_traffic.json")
+    try:
+        rec = json.load(open(path))
+    except Exception:
+        return None
+    entry = rec.get(workload)
+    if not entry or entry.get("kernel_source_hash") != kernel_source_hash():
+        return None
+    return entry.get("dram_bytes_per_launch")
+
+
+# ---------------------------------------------------------------------------
+# GPU arm
+
+class DecodeStep:
+    """Device-resident buffers of one decode workload and the two calls of a step."""
+
+    def __init__(self, w, device, split_tokens=0, kernel="auto"):
+        import paged_kv_decode_pa_gb300 as pa
+
+        self.pa = pa
+        self.w = w
+        self.dev = device
+        self.split = split_tokens
+        self.kernel = kernel
+        self.kc = pa.to_torch(w.k_cache, device)
+        self.vc = pa.to_torch(w.v_cache, device)
+        self.q = pa.to_torch(w.q, device)
+        self.k_new = pa.to_torch(w.k_new, device)
+        self.v_new = pa.to_torch(w.v_new, device)
+        self.slots = pa.to_torch(w.slot_mapping, device)
+        self.tables = pa.to_torch(w.block_tables, device)
+        self.lens = pa.to_torch(w.context_lens, device)
+        self.out = self.q.new_empty(self.q.shape)
+        s = w.spec
+        self.nq = s.num_queries
+        self.ws = pa.new_workspace(s.batch, self.nq, s.q_heads, s.kv_heads, w.max_context_len, device,
+                                   split_tokens)
+
+    def write(self):
+        self.pa.pa_cache_write(self.kc, self.vc, self.k_new, self.v_new, self.slots)
+
+    def attend(self):
+        w = self.w
+        if self.nq == 1:
+            self.pa.pa_decode(self.kc, self.vc, self.q, self.tables, self.lens, w.max_context_len, w.scale,
+                              self.ws, out=self.out, split_tokens=self.split, kernel=self.kernel)
+        else:
+            self.pa.pa_verify(self.kc, self.vc, self.q, self.k_new, self.v_new, self.slots, self.tables,
+                              self.lens, w.max_context_len, w.scale, self.ws, out=self.out,
+                              split_tokens=self.split, kernel=self.kernel)
+
+
+def time_steps(step: DecodeStep, steps: int, warmup: int, flush, with_write=True):
+    """Per-step CUDA-event times (ms) of the whole step and of the attention call."""
+    import torch
+
+    def one():
+        if with_write and step.nq == 1:
+            step.write()
+        step.attend()
+
+    for _ in range(warmup):
+        flush()
+        one()
+    torch.cuda.synchronize()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
+    for k in range(steps):
+        flush()
+        ev[k][0].record()
+        if with_write and step.nq == 1:
+            step.write()
+        ev[k][1].record()
+        step.attend()
+        ev[k][2].record()
+    torch.cuda.synchronize()
+    total = [e[0].elapsed_time(e[2]) for e in ev]
+    attend = [e[1].elapsed_time(e[2]) for e in ev]
+    return total, attend
+
+
+def time_e2e(step: DecodeStep, steps: int, warmup: int, flush):
+    """Same step through the public API from pinned host buffers, copies inside the timed region."""
+    import torch
+
+    pa = step.pa
+    w = step.w
+    host = {name: pa.to_torch(getattr(w, name), "cpu").pin_memory()
+            for name in ("q", "k_new", "v_new", "slot_mapping", "block_tables", "context_lens")}
+    dev = {"q": step.q, "k_new": step.k_new, "v_new": step.v_new, "slot_mapping": step.slots,
+           "block_tables": step.tables, "context_lens": step.lens}
+    out_host = torch.empty(step.out.shape, dtype=step.out.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = out_host.numel() * out_host.element_size()
+
+    def one():
+        for name, t in host.items():
+            dev[name].copy_(t, non_blocking=True)
+        step.write()
+        step.attend()
+        out_host.copy_(step.out, non_blocking=True)
+
+    for _ in range(warmup):
+        flush()
+        one()
+    torch.cuda.synchronize()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(steps)]
+    for k in range(steps):
+        flush()
+        ev[k][0].record()
+        one()
+        ev[k][1].record()
+    torch.cuda.synchronize()
+    return [e[0].elapsed_time(e[1]) for e in ev], h2d, d2h
+
+
+def step_bytes(w):
+    s = w.spec
+    eb = accounting.elem_bytes(s.dtype)
+    att = accounting.decode_bytes(w.context_lens, s.q_heads, s.kv_heads, s.head_dim, eb, s.num_queries)
+    write = accounting.cache_write_bytes(len(w.slot_mapping), s.kv_heads, s.head_dim, eb) if s.num_queries == 1 else 0
+    return att, write
+
+
+def measure_extra(name, device, steps, flush, split, kernel):
+    w = inputs.make(name)
+    st = DecodeStep(w, device, split, kernel)
+    total, attend = time_steps(st, steps, 3, flush)
+    att, _ = step_bytes(w)
+    us = statistics.mean(attend) * 1e3
+    peak, _ = hbm_peak()
+    gbs = att["total"] / (us * 1e-6) / 1e9
+    rec = {"workload": w.spec.description, "us_per_call": round(us, 2),
+           "us_per_call_p10_p90": [round(np.percentile(attend, 10) * 1e3, 2),
+                                   round(np.percentile(attend, 90) * 1e3, 2)],
+           "kv_bytes": att["kv"], "algorithmic_bytes": att["total"],
+           "kv_gbs": round(att["kv"] / (us * 1e-6) / 1e9, 1), "achieved_gbs": round(gbs, 1),
+           "frac_of_measured_hbm": round(gbs / peak, 3), "frac_of_8tbs": round(gbs / 8000.0, 3),
+           "call": "pa_verify (fused write)" if w.spec.num_queries > 1 else "pa_decode",
+           "l2": "flushed before each call"}
+    del st
+    return rec
+
+
+def run_native(args):
+    import torch
+
+    world, rank, local = dist_setup()
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    import paged_kv_decode_pa_gb300 as pa
+    from paged_kv_decode_pa_gb300 import _lib
+
+    _lib.load()  # fails loudly if the library is missing
+    base = inputs.CONFIGS[args.workload]
+    w = inputs.generate(base, seed=base.seed + 1000 * rank)
+    step = DecodeStep(w, device, args.split_tokens, args.kernel)
+    flush_buf = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
+
+    def flush():
+        flush_buf.fill_(1)
+
+    att, write = step_bytes(w)
+    barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clocks:
+        t0 = time.perf_counter()
+        total, attend = time_steps(step, args.steps, args.warmup, flush)
+        wall = time.perf_counter() - t0
+    torch.cuda.synchronize()
+    barrier(world)
+    ms_step = max_over_ranks(statistics.mean(total), world, device)
+    ms_attend = max_over_ranks(statistics.mean(attend), world, device)
+    status = pa.pa_workspace_status(step.ws)
+    if status:
+        raise RuntimeError(f"device status flags {status:#x} during the benchmark")
+
+    e2e_ms, h2d, d2h = time_e2e(step, max(5, args.steps // 2), 3, flush)
+    e2e_step = max_over_ranks(statistics.mean(e2e_ms), world, device)
+
+    kv_total = att["kv"] * world
+    value = kv_total / (ms_step * 1e-3) / 1e9
+    peak, peak_kind = hbm_peak()
+    achieved = att["total"] / (ms_attend * 1e-3) / 1e9
+    traffic = ncu_traffic(args.workload)
+
+    extra = {}
+    if not args.no_extra and rank == 0:
+        for name in ("c2", "c3", "c5"):
+            if name != args.workload:
+                extra[name] = measure_extra(name, device, 20, flush, args.split_tokens, args.kernel)
+
+    cpu = cpu_baseline(w, args.cpu_seconds) if rank == 0 else None
+
+    if rank == 0:
+        s = w.spec
+        line = {
+            "metric": METRIC,
+            "value": round(value, 1),
+            "unit": "GB/s",
+            "n_gpus": world,
+            "steps": args.steps,
+            "warmup": args.warmup,
+            "ms_per_step": round(ms_step, 5),
+            "us_per_call": round(ms_attend * 1e3, 2),
+            "higher_is_better": True,
+            "scaling": "weak",
+            "vs_baseline": None,
+            "dtype": s.dtype,
+            "data": "synthetic (seeded N(0,1) bf16; no dataset or weights involved)",
+            "config": {
+                "workload": f"{args.workload}: {s.description}",
+                "batch": s.batch, "q_heads": s.q_heads, "kv_heads": s.kv_heads, "head_dim": s.head_dim,
+                "block_size": s.block_size, "num_blocks": s.num_blocks,
+                "context_tokens": int(w.context_lens.sum()),
+                "split_tokens": args.split_tokens or _lib.PA_DEFAULT_SPLIT_TOKENS,
+                "kernel": args.kernel,
+                "step": "pa_cache_write (one new token per sequence) + pa_decode",
+                "l2": "flushed before every timed step (256 MiB write, outside the timed region)",
+                "parallelism": f"replicas x{world} (independent sequences per GPU)",
+            },
+            "roofline": {
+                "bound": "hbm",
+                "kernel": "pa_decode (attn_mma_kernel)" if s.dtype == "bf16" and args.kernel != "simt"
+                          else "pa_decode (attn_simt_kernel)",
+                "achieved": round(achieved, 1),
+                "peak": peak,
+                "unit": "GB/s",
+                "frac": round(achieved / peak, 4),
+                "peak_kind": f"{peak_kind} (bf16 copy, read+write)",
+                "frac_of_8tbs_nominal": round(achieved / 8000.0, 4),
+                "algorithmic_bytes_per_launch": att["total"],
+                "traffic": traffic,
+            },
+            "cpu_baseline": cpu,
+            "e2e": {"value": round(kv_total / (e2e_step * 1e-3) / 1e9, 1), "unit": "GB/s",
+                    "ms_per_step": round(e2e_step, 5), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                    "path": "pinned host -> device copies, pa_cache_write, pa_decode, device -> host output"},
+            "gpu_launches": 2 * args.steps,
+            "clocks": clocks.summary(),
+            "wall_s_timed_loop": round(wall, 3),
+            "per_config": extra,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+
+
+# ---------------------------------------------------------------------------
+# CPU baseline: the fp64 oracle, as it stands, on a bounded sample
+
+def cpu_baseline(w, budget_s: float):
+    import oracle
+
+    cores = os.cpu_count() or 1
+    oracle.set_threads(cores)
+    s = w.spec
+    kc, vc = w.k_cache, w.v_cache
+    q = w.q if s.num_queries > 1 else w.q
+    done, elapsed = 0, 0.0
+    chunk = max(1, min(s.batch, cores))
+    used_threads = min(cores, chunk)
+    while done < s.batch and elapsed < budget_s:
+        b1 = min(s.batch, done + chunk)
+        t0 = time.perf_counter()
+        oracle.attend(kc, vc, q if q.ndim == 4 else q, w.block_tables, w.context_lens, w.scale, (done, b1))
+        elapsed += time.perf_counter() - t0
+        done = b1
+    eb = accounting.elem_bytes(s.dtype)
+    kv = accounting.kv_read_bytes(w.context_lens[:done], s.kv_heads, s.head_dim, eb)
+    return {"value": round(kv / elapsed / 1e9, 3), "unit": "GB/s", "cores": used_threads,
+            "kind": "oracle",
+            "sample": f"{done} of {s.batch} sequences ({int(w.context_lens[:done].sum())} tokens), "
+                      f"fp64 C oracle with OpenMP, {elapsed:.2f} s"}
+
+
+def run_reference(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if world > 1 and rank != 0:
+        return
+    import oracle
+
+    cores = os.cpu_count() or 1
+    oracle.set_threads(cores)
+    base = inputs.CONFIGS[args.workload]
+    w = inputs.generate(base)
+    s = w.spec
+    # One step = the oracle on a bounded sample of the sequences (one per core).
+    sample = max(1, min(s.batch, cores))
+    per_step_budget = 120.0 / max(1, args.steps + args.warmup)
+    times = []
+    for k in range(args.warmup + args.steps):
+        t0 = time.perf_counter()
+        n = 0
+        while n < s.batch:
+            b1 = min(s.batch, n + sample)
+            oracle.attend(w.k_cache, w.v_cache, w.q, w.block_tables, w.context_lens, w.scale, (n, b1))
+            n = b1
+            if time.perf_counter() - t0 > per_step_budget:
+                break
+        dt = time.perf_counter() - t0
+        if k >= args.warmup:
+            times.append((dt, n))
+    eb = accounting.elem_bytes(s.dtype)
+    total_t = sum(t for t, _ in times)
+    total_kv = sum(accounting.kv_read_bytes(w.context_lens[:n], s.kv_heads, s.head_dim, eb) for _, n in times)
+    value = total_kv / total_t / 1e9
+    ms = total_t / len(times) * 1e3
+    line = {
+        "impl": "reference",
+        "metric": METRIC, "value": round(value, 3), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded N(0,1) bf16)",
+        "config": {"workload": f"{args.workload}: {s.description}",
+                   "step": "fp64 CPU oracle attention over a bounded sample of the sequences"},
+        "cpu_baseline": {"value": round(value, 3), "unit": "GB/s", "cores": min(cores, sample),
+                         "kind": "oracle", "sample": f"up to {per_step_budget:.1f} s of sequences per step"},
+        "e2e": {"value": round(value, 3), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_native(args)
+
+
+if __name__ == "__main__":
+    main()

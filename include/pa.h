@@ -1,0 +1,243 @@
+/*
+ * pa.h: C ABI of libpa, decode-time attention over a paged KV cache on one
+ * NVIDIA GB300 (sm_103a).
+ *
+ * Three operations, all asynchronous on the caller's CUDA stream:
+ *
+ *   pa_cache_write  slot-mapping scatter of new K/V rows into the block pool;
+ *   pa_decode       grouped-query attention of one query token per sequence
+ *                   over that sequence's cached context, read in place
+ *                   through its block table;
+ *   pa_verify       the k+1-token speculative-verify variant: writes the new
+ *                   tokens' K/V and attends with a causal mask among them.
+ *
+ * Where each operation is defined:
+ *  - The cache is head-major, [kv_heads, num_blocks, block_size, head_dim], so
+ *    one index over a sequence's slots returns its context in order ("From
+ *    183 ms to 19 ms per decode step", section "2. Head-major KV cache").
+ *  - Decode walks each sequence's block table and reads K and V straight from
+ *    the cache, one (sequence, KV head) with its whole query-head group at a
+ *    time, with an online softmax in fp32 (same page, section "3. A Triton
+ *    paged-decode kernel"). Query head hq reads KV head hq / (q_heads /
+ *    kv_heads) (same page, section "1. Grouped attention").
+ *  - Each step's per-token inputs are cache slots, block tables and context
+ *    lengths, copied into fixed buffers so the calls can be captured in a CUDA
+ *    graph (same page, section "4. CUDA graphs per batch bucket").
+ *  - Verify carries k+1 query tokens per sequence with a causal mask among
+ *    them (same page, section "Then speculative decoding got slower").
+ *  - A zero key is not neutral, so every key beyond a sequence's length is
+ *    masked, scores and values both ("A Rust inference server for Qwen2 on
+ *    Apple Silicon", Day 3 "Known gaps").
+ *
+ * Conventions shared by every call:
+ *  - Pointers named d_* or documented as "device" point to device memory of
+ *    the current device; all arrays are C-contiguous. Element pointers (cache,
+ *    q, out, k_new, v_new) must be 16-byte aligned.
+ *  - The caller owns every buffer, including the workspace. The library
+ *    allocates nothing, frees nothing and keeps no pointer after a call
+ *    returns. Buffers must stay alive until the stream reaches the call (a
+ *    captured graph keeps reading the same addresses on every replay).
+ *  - Calls never synchronise the host and never read device memory on the
+ *    host; the launch grid depends on host arguments only, so every call can
+ *    be captured in a CUDA graph.
+ *  - Arguments the host can check are checked before anything is launched; a
+ *    failing check returns an error status and nothing is written.
+ *  - Device-resident indices (block ids, context lengths, slots) are the
+ *    caller's contract. Kernels never read or write outside the cache for a
+ *    bad index: a block id outside [0, num_blocks) reads zeros, a slot outside
+ *    the pool is skipped, a length above the limits is clamped; each such
+ *    event raises a bit in the workspace status word (pa_workspace_status)
+ *    where a workspace is passed. pa_validate reports them without attending.
+ *  - Kernels contain no trap and no unbounded wait. A wait that exceeds its
+ *    limit raises PA_FLAG_TIMEOUT and the kernel returns.
+ *
+ * Supported shapes: head_dim 128, block_size 16, dtype bf16 or fp32,
+ * q_heads a multiple of kv_heads.
+ */
+#ifndef PA_H_
+#define PA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Element type of caches, queries, new rows and outputs (all the same). */
+typedef enum pa_dtype {
+    PA_DTYPE_F32 = 0,
+    PA_DTYPE_BF16 = 1
+} pa_dtype;
+
+typedef enum pa_status {
+    PA_OK = 0,
+    PA_ERR_INVALID_ARG = 1, /* null or misaligned pointer, negative size, inconsistent shapes */
+    PA_ERR_UNSUPPORTED = 2, /* head_dim != 128, block_size != 16, unknown dtype, option out of range */
+    PA_ERR_WORKSPACE = 3,   /* workspace missing or smaller than pa_workspace_size() */
+    PA_ERR_CUDA = 4         /* a CUDA runtime/driver call failed; see pa_last_cuda_error() */
+} pa_status;
+
+/* Bits of the device status word in the workspace (pa_workspace_status). */
+#define PA_FLAG_BAD_BLOCK 0x1u   /* a block id outside [0, num_blocks) was met (zeros were read) */
+#define PA_FLAG_BAD_LENGTH 0x2u  /* a context length < 0, > max_context_len or > table capacity (clamped) */
+#define PA_FLAG_BAD_SLOT 0x4u    /* a slot >= num_blocks * block_size (the write was skipped) */
+#define PA_FLAG_TIMEOUT 0x8u     /* a bounded wait gave up; results of that call are not valid */
+
+/* The block pool: two head-major tensors [kv_heads, num_blocks, block_size,
+ * head_dim] of `dtype`, device memory, 16-byte aligned. */
+typedef struct pa_cache {
+    void *k;
+    void *v;
+    int32_t kv_heads;
+    int32_t num_blocks;
+    int32_t block_size; /* must be 16 */
+    int32_t head_dim;   /* must be 128 */
+    int32_t dtype;      /* pa_dtype */
+} pa_cache;
+
+/* Kernel choice for pa_decode / pa_verify. */
+typedef enum pa_kernel {
+    PA_KERNEL_AUTO = 0, /* bf16: tensor-core kernel; fp32: CUDA-core kernel */
+    PA_KERNEL_MMA = 1,  /* bf16 only: TMA-staged tiles, bf16 tensor-core products, fp32 softmax */
+    PA_KERNEL_SIMT = 2  /* CUDA-core fp32 arithmetic, any dtype (kept for comparison and fp32) */
+} pa_kernel;
+
+/* Optional tuning for pa_decode / pa_verify; pass NULL for the defaults. */
+typedef struct pa_options {
+    /* Tokens per context split (flash-decoding split-K). 0 = default
+     * (PA_DEFAULT_SPLIT_TOKENS). Must be a positive multiple of block_size.
+     * A sequence's result depends only on its own length and this value, never
+     * on its batch-mates, so it is bit-identical across batch compositions. */
+    int32_t split_tokens;
+    int32_t kernel; /* pa_kernel */
+} pa_options;
+
+#define PA_DEFAULT_SPLIT_TOKENS 512
+
+/*
+ * pa_cache_write: cache[h, s / 16, s % 16, :] = new[i, h, :] for every token
+ * i with slot s = slot_mapping[i] >= 0, for both K and V, copied bit for bit.
+ * Defined by the per-step "cache slots" input ("From 183 ms to 19 ms per
+ * decode step", section "4. CUDA graphs per batch bucket") and the
+ * write-before-attend order of a decode step ("Anatomy of a Decode-Step
+ * Stall", the engine's Model._layer).
+ *
+ *   cache         the pool (device tensors written in place).
+ *   d_k_new, d_v_new  [num_tokens, kv_heads, head_dim] of cache->dtype, device.
+ *   d_slot_mapping    [num_tokens] int32, device. s < 0: token skipped.
+ *                     s >= num_blocks*16: skipped (no status word here; use
+ *                     pa_validate to find it). Duplicate slots: unspecified
+ *                     which write lands.
+ *   num_tokens    >= 0; 0 launches nothing.
+ *   stream        cudaStream_t (NULL = legacy default stream).
+ * Returns PA_OK or an error status (nothing launched on error).
+ */
+pa_status pa_cache_write(const pa_cache *cache, const void *d_k_new, const void *d_v_new,
+                         const int32_t *d_slot_mapping, int32_t num_tokens, void *stream);
+
+/*
+ * Bytes of workspace pa_decode / pa_verify need for these sizes. The workspace
+ * holds a status word, one arrival counter per (sequence, KV head, row group)
+ * and the fp32 split partials. It must be zero-filled once before first use
+ * (pa_workspace_init); every call leaves it ready for the next.
+ * num_queries is 1 for decode. Returns 0 if an argument is invalid.
+ */
+size_t pa_workspace_size(int32_t batch, int32_t num_queries, int32_t q_heads, int32_t kv_heads,
+                         int32_t head_dim, int32_t max_context_len, const pa_options *opts);
+
+/* Zero-fill a workspace on `stream` (asynchronous). */
+pa_status pa_workspace_init(void *d_workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * Read and clear the workspace status word (PA_FLAG_* bits). Synchronises
+ * `stream` and copies 4 bytes to the host: a diagnostic, not for the hot path.
+ */
+pa_status pa_workspace_status(void *d_workspace, uint32_t *host_flags, void *stream);
+
+/*
+ * pa_decode: for every sequence b and query head hq (KV head h = hq / G,
+ * G = q_heads / kv_heads), with L = context_lens[b],
+ *     s_t = scale * <q[b, hq, :], K[h, t, :]>            for t < L,
+ *     out[b, hq, :] = sum_t softmax(s)_t * V[h, t, :],
+ * where K[h, t, :] = cache.k[h, block_tables[b][t / 16], t % 16, :]
+ * ("From 183 ms to 19 ms per decode step", sections "1. Grouped attention",
+ * "2. Head-major KV cache", "3. A Triton paged-decode kernel"). L = 0 gives
+ * zeros. The softmax runs in fp32 with a running max and sum; products of bf16
+ * inputs accumulate in fp32; out is rounded to the cache dtype.
+ *
+ *   cache          the pool (read only).
+ *   d_q            [batch, q_heads, head_dim], device.
+ *   d_out          [batch, q_heads, head_dim], device; must not overlap inputs.
+ *   d_block_tables [batch, max_blocks_per_seq] int32, device. Entries at or
+ *                  beyond ceil(L/16) are never read.
+ *   d_context_lens [batch] int32, device; each in [0, max_context_len] and
+ *                  <= max_blocks_per_seq * 16 (else clamped and flagged).
+ *   max_context_len host-side upper bound of context_lens; sizes the grid.
+ *   scale          softmax scale (1/sqrt(head_dim) for the standard form).
+ *   d_workspace    >= pa_workspace_size(batch, 1, ...) bytes, zeroed once.
+ *   opts           NULL or pa_options.
+ */
+pa_status pa_decode(const pa_cache *cache, const void *d_q, void *d_out,
+                    const int32_t *d_block_tables, int32_t max_blocks_per_seq,
+                    const int32_t *d_context_lens, int32_t batch, int32_t q_heads,
+                    int32_t max_context_len, float scale, void *d_workspace,
+                    size_t workspace_bytes, const pa_options *opts, void *stream);
+
+/*
+ * pa_verify: one fused call of the speculative-verify step. The num_queries
+ * new tokens of sequence b sit at positions L - num_queries + i (L =
+ * context_lens[b] counts them). Their K/V rows are written to the cache at
+ * slot_mapping[b * num_queries + i], and query i attends to positions
+ * t <= L - num_queries + i (causal among the new tokens; "From 183 ms to 19 ms
+ * per decode step", section "Then speculative decoding got slower"). The
+ * result equals pa_cache_write followed by attention over the updated cache,
+ * provided each slot is the table slot of its position (pa_validate checks
+ * this); the attention reads the new rows from d_k_new / d_v_new directly.
+ * A row whose position is negative returns zeros. Padded query rows are
+ * computed like any other and may be discarded by the caller.
+ *
+ *   d_q, d_out     [batch, num_queries, q_heads, head_dim], device.
+ *   d_k_new, d_v_new [batch * num_queries, kv_heads, head_dim], device.
+ *   d_slot_mapping [batch * num_queries] int32, device.
+ *   Other arguments as in pa_decode; the cache is written in place.
+ */
+pa_status pa_verify(const pa_cache *cache, const void *d_q, void *d_out, const void *d_k_new,
+                    const void *d_v_new, const int32_t *d_slot_mapping, int32_t num_queries,
+                    const int32_t *d_block_tables, int32_t max_blocks_per_seq,
+                    const int32_t *d_context_lens, int32_t batch, int32_t q_heads,
+                    int32_t max_context_len, float scale, void *d_workspace,
+                    size_t workspace_bytes, const pa_options *opts, void *stream);
+
+/*
+ * pa_validate: check the device-resident per-step inputs without attending.
+ * Writes a report of PA_VALIDATE_WORDS uint32 words to d_report (device):
+ *   [0] PA_FLAG_* bits found;
+ *   [1] count of sequences with a bad length (< 0, > max_context_len,
+ *       > max_blocks_per_seq * 16, or < num_queries when num_queries > 1);
+ *   [2] count of block-table entries in use outside [0, num_blocks);
+ *   [3] count of slots outside [-1, num_blocks * 16) or not equal to the
+ *       table slot of their position (only when d_slot_mapping is non-NULL).
+ * d_slot_mapping may be NULL; it then holds batch * num_queries entries
+ * otherwise. Never traps; graph-capturable.
+ */
+#define PA_VALIDATE_WORDS 4
+pa_status pa_validate(const pa_cache *cache, const int32_t *d_block_tables,
+                      int32_t max_blocks_per_seq, const int32_t *d_context_lens, int32_t batch,
+                      int32_t max_context_len, const int32_t *d_slot_mapping,
+                      int32_t num_queries, uint32_t *d_report, void *stream);
+
+/* Human-readable name of a status. */
+const char *pa_status_string(pa_status status);
+
+/* The last CUDA error code seen by a call that returned PA_ERR_CUDA (0 if none). */
+int pa_last_cuda_error(void);
+
+/* Library version as major * 10000 + minor * 100 + patch. */
+int pa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PA_H_ */

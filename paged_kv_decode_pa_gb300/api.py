@@ -1,0 +1,180 @@
+"""Python binding of libpa: the C entry points under the same names, taking torch tensors.
+
+Argument marshalling only. Every operation runs in libpa's CUDA kernels on the
+caller's current CUDA stream (or the one passed). PyTorch provides device
+memory and streams; nothing here computes attention.
+"""
+
+from __future__ import annotations
+
+import ctypes
+from typing import Optional
+
+import numpy as np
+import torch
+
+from . import _lib as L
+
+_DTYPES = {torch.bfloat16: L.PA_DTYPE_BF16, torch.float32: L.PA_DTYPE_F32}
+_KERNELS = {"auto": L.PA_KERNEL_AUTO, "mma": L.PA_KERNEL_MMA, "simt": L.PA_KERNEL_SIMT}
+
+
+def _vp(t: Optional[torch.Tensor]):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else ctypes.c_void_p(None)
+
+
+def _stream(stream: Optional[torch.cuda.Stream]):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _need(cond: bool, msg: str):
+    if not cond:
+        raise ValueError(msg)
+
+
+def make_cache(k_cache: torch.Tensor, v_cache: torch.Tensor) -> L.PaCache:
+    """Describe two head-major pools [kv_heads, num_blocks, block_size, head_dim]."""
+    _need(k_cache.shape == v_cache.shape and k_cache.dim() == 4, "caches must be equal 4-D tensors")
+    _need(k_cache.dtype == v_cache.dtype and k_cache.dtype in _DTYPES, "cache dtype must be bf16 or fp32")
+    _need(k_cache.is_cuda and v_cache.is_cuda, "caches must be CUDA tensors")
+    _need(k_cache.is_contiguous() and v_cache.is_contiguous(), "caches must be contiguous")
+    hkv, nb, bs, d = k_cache.shape
+    return L.PaCache(k_cache.data_ptr(), v_cache.data_ptr(), hkv, nb, bs, d, _DTYPES[k_cache.dtype])
+
+
+def _options(split_tokens: int, kernel: str) -> L.PaOptions:
+    return L.PaOptions(int(split_tokens), _KERNELS[kernel])
+
+
+def pa_workspace_size(batch: int, num_queries: int, q_heads: int, kv_heads: int,
+                      max_context_len: int, split_tokens: int = 0, head_dim: int = 128) -> int:
+    opts = _options(split_tokens, "auto")
+    n = L.load().pa_workspace_size(batch, num_queries, q_heads, kv_heads, head_dim,
+                                   max_context_len, ctypes.byref(opts))
+    if n == 0:
+        raise ValueError("pa_workspace_size: invalid sizes")
+    return int(n)
+
+
+def pa_workspace_init(workspace: torch.Tensor, stream=None) -> None:
+    L.check("pa_workspace_init", L.load().pa_workspace_init(
+        _vp(workspace), workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def new_workspace(batch: int, num_queries: int, q_heads: int, kv_heads: int, max_context_len: int,
+                  device="cuda", split_tokens: int = 0, stream=None) -> torch.Tensor:
+    """Allocate (torch) and zero (libpa) a workspace for these sizes."""
+    n = pa_workspace_size(batch, num_queries, q_heads, kv_heads, max_context_len, split_tokens)
+    ws = torch.empty(n, dtype=torch.uint8, device=device)
+    pa_workspace_init(ws, stream)
+    return ws
+
+
+def pa_workspace_status(workspace: torch.Tensor, stream=None) -> int:
+    """Read and clear the PA_FLAG_* status word (synchronises the stream)."""
+    flags = ctypes.c_uint32(0)
+    L.check("pa_workspace_status", L.load().pa_workspace_status(
+        _vp(workspace), ctypes.byref(flags), _stream(stream)))
+    return int(flags.value)
+
+
+def pa_cache_write(k_cache, v_cache, k_new, v_new, slot_mapping, stream=None) -> None:
+    cache = make_cache(k_cache, v_cache)
+    n = int(slot_mapping.shape[0])
+    _need(slot_mapping.dtype == torch.int32, "slot_mapping must be int32")
+    _need(k_new.dtype == k_cache.dtype and v_new.dtype == k_cache.dtype, "new rows must match the cache dtype")
+    _need(tuple(k_new.shape) == (n, cache.kv_heads, cache.head_dim) and k_new.shape == v_new.shape,
+          "new rows must be [num_tokens, kv_heads, head_dim]")
+    _need(k_new.is_contiguous() and v_new.is_contiguous() and slot_mapping.is_contiguous(),
+          "inputs must be contiguous")
+    L.check("pa_cache_write", L.load().pa_cache_write(
+        ctypes.byref(cache), _vp(k_new), _vp(v_new), _vp(slot_mapping), n, _stream(stream)))
+
+
+def _tables(block_tables, context_lens, batch):
+    _need(block_tables.dtype == torch.int32 and context_lens.dtype == torch.int32,
+          "block_tables and context_lens must be int32")
+    _need(block_tables.dim() == 2 and block_tables.shape[0] == batch, "block_tables must be [batch, mbps]")
+    _need(tuple(context_lens.shape) == (batch,), "context_lens must be [batch]")
+    _need(block_tables.is_contiguous() and context_lens.is_contiguous(), "tables must be contiguous")
+    return int(block_tables.shape[1])
+
+
+def pa_decode(k_cache, v_cache, q, block_tables, context_lens, max_context_len: int, scale: float,
+              workspace, out=None, split_tokens: int = 0, kernel: str = "auto", stream=None):
+    """out[b, hq] = softmax(scale * q[b, hq] . K_b^T) V_b over sequence b's paged context."""
+    cache = make_cache(k_cache, v_cache)
+    _need(q.dim() == 3 and q.dtype == k_cache.dtype and q.is_contiguous(), "q must be [batch, q_heads, head_dim]")
+    batch, q_heads, _ = q.shape
+    mbps = _tables(block_tables, context_lens, batch)
+    if out is None:
+        out = torch.empty_like(q)
+    opts = _options(split_tokens, kernel)
+    L.check("pa_decode", L.load().pa_decode(
+        ctypes.byref(cache), _vp(q), _vp(out), _vp(block_tables), mbps, _vp(context_lens), batch,
+        q_heads, int(max_context_len), float(scale), _vp(workspace),
+        workspace.numel() * workspace.element_size(), ctypes.byref(opts), _stream(stream)))
+    return out
+
+
+def pa_verify(k_cache, v_cache, q, k_new, v_new, slot_mapping, block_tables, context_lens,
+              max_context_len: int, scale: float, workspace, out=None, split_tokens: int = 0,
+              kernel: str = "auto", stream=None):
+    """Fused speculative verify: write the new K/V, attend causally. q: [batch, nq, q_heads, head_dim]."""
+    cache = make_cache(k_cache, v_cache)
+    _need(q.dim() == 4 and q.dtype == k_cache.dtype and q.is_contiguous(),
+          "q must be [batch, num_queries, q_heads, head_dim]")
+    batch, nq, q_heads, _ = q.shape
+    mbps = _tables(block_tables, context_lens, batch)
+    _need(slot_mapping.dtype == torch.int32 and tuple(slot_mapping.shape) == (batch * nq,),
+          "slot_mapping must be int32 [batch * num_queries]")
+    _need(tuple(k_new.shape) == (batch * nq, cache.kv_heads, cache.head_dim) and k_new.shape == v_new.shape
+          and k_new.dtype == k_cache.dtype and v_new.dtype == k_cache.dtype,
+          "new rows must be [batch * num_queries, kv_heads, head_dim] of the cache dtype")
+    if out is None:
+        out = torch.empty_like(q)
+    opts = _options(split_tokens, kernel)
+    L.check("pa_verify", L.load().pa_verify(
+        ctypes.byref(cache), _vp(q), _vp(out), _vp(k_new), _vp(v_new), _vp(slot_mapping), nq,
+        _vp(block_tables), mbps, _vp(context_lens), batch, q_heads, int(max_context_len),
+        float(scale), _vp(workspace), workspace.numel() * workspace.element_size(),
+        ctypes.byref(opts), _stream(stream)))
+    return out
+
+
+def pa_validate(k_cache, v_cache, block_tables, context_lens, max_context_len: int,
+                slot_mapping=None, num_queries: int = 1, report=None, stream=None):
+    """Device check of tables, lengths and slots; returns the 4-word report tensor (int32 view)."""
+    cache = make_cache(k_cache, v_cache)
+    batch = int(context_lens.shape[0])
+    mbps = _tables(block_tables, context_lens, batch)
+    if report is None:
+        report = torch.zeros(L.PA_VALIDATE_WORDS, dtype=torch.int32, device=k_cache.device)
+    L.check("pa_validate", L.load().pa_validate(
+        ctypes.byref(cache), _vp(block_tables), mbps, _vp(context_lens), batch, int(max_context_len),
+        _vp(slot_mapping), int(num_queries), _vp(report), _stream(stream)))
+    return report
+
+
+def pa_status_string(status: int) -> str:
+    return L.load().pa_status_string(int(status)).decode()
+
+
+def pa_version() -> int:
+    return int(L.load().pa_version())
+
+
+def to_torch(arr: np.ndarray, device="cuda") -> torch.Tensor:
+    """Copy a host array to the device; uint16 arrays are bf16 bit patterns."""
+    if arr.dtype == np.uint16:
+        return torch.from_numpy(np.ascontiguousarray(arr).view(np.int16)).view(torch.bfloat16).to(device)
+    return torch.from_numpy(np.ascontiguousarray(arr)).to(device)
+
+
+def to_numpy(t: torch.Tensor) -> np.ndarray:
+    """Copy a device tensor to the host; bf16 comes back as uint16 bit patterns."""
+    t = t.detach().cpu().contiguous()
+    if t.dtype == torch.bfloat16:
+        return t.view(torch.int16).numpy().view(np.uint16)
+    return t.numpy()

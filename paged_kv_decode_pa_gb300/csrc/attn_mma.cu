@@ -1,0 +1,413 @@
+// Paged decode / verify attention, bf16, tensor-core products (sm_103a).
+//
+// One CTA per (context split, KV head, sequence x row group), holding every
+// query row of the group that reads this KV head: the query-head group for
+// decode, (k+1) x group rows for verify ("From 183 ms to 19 ms per decode
+// step", sections "1. Grouped attention", "3. A Triton paged-decode kernel",
+// "Then speculative decoding got slower"). The split is a fixed number of
+// tokens, so a sequence's result depends on its own length only.
+//
+// Warp roles (5 warps):
+//   warp 4      producer: one lane walks the split's block-table entries and
+//               issues TMA tensor loads of each 16-token block, K and V, into a
+//               ring of shared-memory stages (128-byte swizzle, so ldmatrix
+//               reads are bank-conflict free). Each block is a contiguous
+//               16 x 128 tile of the head-major cache ("2. Head-major KV
+//               cache"): no gather, no padded copy.
+//   warps 0..3  consumers: block j goes to warp j % 4. Per block, a warp
+//               computes S^T = K Q^T (16 tokens x up to 16 rows) with
+//               m16n8k16 bf16 MMAs, masks, runs the fp32 online softmax
+//               (running max and sum, rescaled per block: "3. A Triton
+//               paged-decode kernel"), turns P^T into the B operand in
+//               registers (movmatrix; P split into two bf16 parts), and
+//               accumulates O^T += V^T P^T.
+// Then the four warps' states are combined and the split epilogue writes the
+// output, or a partial plus the log-sum-exp that the last split merges.
+//
+// Masking: a position beyond the sequence (or beyond a verify row's causal
+// limit) gets score -inf, and the V rows of a partial last block are zeroed in
+// shared memory before use, since stale rows may hold anything ("A Rust
+// inference server for Qwen2 on Apple Silicon", Day 3 "Known gaps": a zero key
+// is not neutral; 0 x NaN is NaN).
+//
+// Fused verify: the CTA whose split holds a new token's position writes that
+// token's K/V row to the cache (row group 0 only) and patches the row into its
+// shared-memory tile from the inputs, so no CTA depends on another's write.
+#include "pa_device.cuh"
+
+namespace pa {
+
+constexpr int kStages = 8;              // shared-memory ring depth (blocks in flight per CTA)
+constexpr int kTileBytes = 16 * 128 * 2;  // one 16-token bf16 tile of K or V
+constexpr int kHalfTile = kTileBytes / 2;  // one TMA box: 16 rows x 64 dims, 128-byte swizzled
+constexpr int kStageBytes = 2 * kTileBytes;
+constexpr int kMmaThreads = (kConsumerWarps + 1) * 32;
+
+struct MmaSmem {
+  // Offsets from the 1024-byte aligned base.
+  static constexpr int stages = 0;
+  static constexpr int bars = kStages * kStageBytes;            // full[kStages], empty[kStages]
+  static constexpr int ids = bars + 2 * kStages * 8;            // block ids of the split
+  static constexpr int ml = ids + (kMaxSplitTokens / kBlockSize) * 4;  // m, l per warp and row
+  static constexpr int flag = ml + 2 * kConsumerWarps * kRowSlots * 4;
+  static constexpr int total = flag + 16;
+  static constexpr int alloc = total + 1024;  // slack for aligning the base
+};
+static_assert(kConsumerWarps * kRowSlots * kCombineStride * 4 <= kStages * kStageBytes,
+              "cross-warp buffer must fit in the stage ring");
+
+// Byte offset of (token row t, 16-byte chunk c of 16) inside a K or V tile:
+// chunk c lives in box c / 8; within a box, 128-byte rows are swizzled by
+// XOR-ing the chunk index with (row & 7).
+__device__ __forceinline__ uint32_t tile_off(int t, int c) {
+  return uint32_t((c >> 3) * kHalfTile + t * 128 + (((c & 7) ^ (t & 7)) << 4));
+}
+
+template <int NT>
+__global__ void __launch_bounds__(kMmaThreads, NT == 1 ? 3 : 2)
+    attn_mma_kernel(const __grid_constant__ CUtensorMap tmap_k,
+                    const __grid_constant__ CUtensorMap tmap_v, const AttnParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* sbase = smem_raw + (base - raw);
+  int32_t* s_ids = reinterpret_cast<int32_t*>(sbase + MmaSmem::ids);
+  float* s_m = reinterpret_cast<float*>(sbase + MmaSmem::ml);
+  float* s_l = s_m + kConsumerWarps * kRowSlots;
+  int* s_flag = reinterpret_cast<int*>(sbase + MmaSmem::flag);
+  const uint32_t bar_full = base + MmaSmem::bars;
+  const uint32_t bar_empty = bar_full + kStages * 8;
+
+  const CtaWork w = cta_work(p);
+  if (w.split >= w.nsplit) {
+    if (w.L == 0 && w.split == 0) write_zero_rows<uint16_t>(p, w);
+    return;
+  }
+  const int nblk = (w.t1 - w.t0 + kBlockSize - 1) / kBlockSize;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  // Block ids of this split; a bad id is replaced by a coordinate outside the
+  // tensor, which TMA fills with zeros.
+  for (int j = threadIdx.x; j < nblk; j += blockDim.x) {
+    int id = __ldg(p.block_tables + int64_t(w.b) * p.mbps + w.t0 / kBlockSize + j);
+    if (id < 0 || id >= p.num_blocks) {
+      raise_flag(p.status, PA_FLAG_BAD_BLOCK);
+      id = -1;
+    }
+    s_ids[j] = id;
+  }
+  if (threadIdx.x == 0) {
+    s_flag[0] = s_flag[1] = s_flag[2] = s_flag[3] = 0;
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(bar_full + 8 * s, 1);
+      mbar_init(bar_empty + 8 * s, 1);
+    }
+    fence_mbar_init();
+  }
+  __syncthreads();
+
+  // Consumer state lives at function scope so that it survives until the
+  // combine below (the producer warp carries an unused copy).
+  float o[8][NT][4];
+  float m_run[NT][2], l_run[NT][2];
+#pragma unroll
+  for (int mt = 0; mt < 8; ++mt)
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) o[mt][nt][e] = 0.f;
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      m_run[nt][e] = -INFINITY;
+      l_run[nt][e] = 0.f;
+    }
+  const int g = lane >> 2;  // MMA group id
+  const int c = lane & 3;   // thread in group
+
+  if (warp == kConsumerWarps) {
+    // ---------------- producer ----------------
+    if (lane == 0) {
+      prefetch_tensormap(&tmap_k);
+      prefetch_tensormap(&tmap_v);
+      const uint64_t policy = policy_evict_first();
+      int issued = 0;
+      for (int j = 0; j < nblk; ++j) {
+        const int s = j % kStages, n = j / kStages;
+        if (n > 0 && !mbar_wait(bar_empty + 8 * s, (n - 1) & 1)) {
+          raise_flag(p.status, PA_FLAG_TIMEOUT);
+          s_flag[2] = 1;
+          break;
+        }
+        const uint32_t st = base + MmaSmem::stages + s * kStageBytes;
+        const uint32_t fb = bar_full + 8 * s;
+        const int id = s_ids[j];
+        const int y = id >= 0 ? id * kBlockSize : -kBlockSize;
+        mbar_arrive_expect_tx(fb, kStageBytes);
+        tma_load_3d(st, &tmap_k, 0, y, w.h, fb, policy);
+        tma_load_3d(st + kHalfTile, &tmap_k, 64, y, w.h, fb, policy);
+        tma_load_3d(st + kTileBytes, &tmap_v, 0, y, w.h, fb, policy);
+        tma_load_3d(st + kTileBytes + kHalfTile, &tmap_v, 64, y, w.h, fb, policy);
+        issued = j + 1;
+      }
+      s_flag[1] = issued;
+    }
+  } else {
+    // ---------------- consumers ----------------
+    // Q^T as the B operand of S^T = K Q^T, kept in registers for the split:
+    // qb[kk][nt][0] holds row nt*8+g, dims 16kk + 2c, +1; [1] dims +8.
+    uint32_t qb[8][NT][2];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      const int r = nt * 8 + g;
+      const bool live = r < w.nrows;
+      const uint32_t* qrow =
+          reinterpret_cast<const uint32_t*>(static_cast<const uint16_t*>(p.q) +
+                                            row_offset(p, w.b, w.h, w.row0 + (live ? r : 0)));
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk) {
+        qb[kk][nt][0] = live ? __ldg(qrow + kk * 8 + c) : 0u;
+        qb[kk][nt][1] = live ? __ldg(qrow + kk * 8 + 4 + c) : 0u;
+      }
+    }
+    // Causal limit of this thread's rows (nt*8 + 2c + e); rows past the group
+    // get -1, i.e. fully masked.
+    int limit[NT][2];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int r = nt * 8 + 2 * c + e;
+        limit[nt][e] = r < w.nrows ? row_limit(p, w.L, w.row0 + r) : -1;
+      }
+
+    // ldmatrix lane roles: matrix mi = lane / 8, row rr = lane % 8.
+    const int mi = lane >> 3, rr = lane & 7;
+    const int k_tok = (mi & 1) * 8 + rr, k_chunk = mi >> 1;  // K as A: (tokens, dims)
+    const int v_tok = (mi >> 1) * 8 + rr, v_chunk = mi & 1;  // V^T as A via .trans
+    const int new0 = w.L - p.num_queries;  // first position of a new (verify) token
+
+    for (int j = warp; j < nblk; j += kConsumerWarps) {
+      const int s = j % kStages;
+      if (!mbar_wait(bar_full + 8 * s, (j / kStages) & 1)) {
+        raise_flag(p.status, PA_FLAG_TIMEOUT);
+        s_flag[2] = 1;
+        break;
+      }
+      const uint32_t kt = base + MmaSmem::stages + s * kStageBytes;
+      const uint32_t vt = kt + kTileBytes;
+      uint8_t* kt_ptr = sbase + MmaSmem::stages + s * kStageBytes;
+      uint8_t* vt_ptr = kt_ptr + kTileBytes;
+      const int tok0 = w.t0 + j * kBlockSize;
+
+      // Fix the tile up in shared memory before reading it.
+      bool patched = false;
+      const int valid = min(kBlockSize, w.L - tok0);  // rows of this block inside the context
+      if (p.fused_write && tok0 + kBlockSize > new0) {
+        // New tokens: K/V come from the inputs; row group 0 also writes them
+        // to the cache. Lanes 0..15 move K chunks, lanes 16..31 V chunks.
+        const int pos_lo = max(tok0, new0), pos_hi = min(tok0 + kBlockSize, w.L);
+        const int ch = lane & 15;
+        const bool is_v = lane >= 16;
+        for (int pos = pos_lo; pos < pos_hi; ++pos) {
+          const int i = pos - new0;
+          const int t = pos - tok0;
+          const int64_t src =
+              (int64_t(w.b * p.num_queries + i) * p.kv_heads + w.h) * kHeadDim + ch * 8;
+          const uint16_t* srcp = static_cast<const uint16_t*>(is_v ? p.v_new : p.k_new) + src;
+          const uint4 val = __ldg(reinterpret_cast<const uint4*>(srcp));
+          *reinterpret_cast<uint4*>((is_v ? vt_ptr : kt_ptr) + tile_off(t, ch)) = val;
+          if (w.rg == 0) {
+            const int slot = __ldg(p.slot_mapping + w.b * p.num_queries + i);
+            if (slot >= 0 && slot < p.num_blocks * kBlockSize) {
+              const int64_t dst = ((int64_t(w.h) * p.num_blocks + slot / kBlockSize) * kBlockSize +
+                                   slot % kBlockSize) * kHeadDim + ch * 8;
+              uint16_t* cache = static_cast<uint16_t*>(is_v ? p.v_cache_w : p.k_cache_w);
+              *reinterpret_cast<uint4*>(cache + dst) = val;
+            } else if (slot >= 0 && lane == 0) {
+              raise_flag(p.status, PA_FLAG_BAD_SLOT);
+            }
+          }
+        }
+        patched = true;
+      }
+      if (valid < kBlockSize) {
+        // Rows beyond the context: zero V so that 0 x (stale row) stays 0.
+        for (int e = lane; e < (kBlockSize - valid) * 16; e += 32) {
+          const int t = valid + (e >> 4), ch = e & 15;
+          *reinterpret_cast<uint4*>(vt_ptr + tile_off(t, ch)) = make_uint4(0, 0, 0, 0);
+        }
+        patched = true;
+      }
+      if (patched) __syncwarp();
+
+      // S^T (16 tokens x 8*NT rows) = K (16 x 128) . Q^T (128 x 8*NT)
+      float sc[NT][4];
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) sc[nt][e] = 0.f;
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk) {
+        uint32_t a[4];
+        ldsm_x4(kt + tile_off(k_tok, 2 * kk + k_chunk), a[0], a[1], a[2], a[3]);
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) mma_bf16_16816(sc[nt], a, qb[kk][nt][0], qb[kk][nt][1]);
+      }
+
+      // Scale to base-2 units and mask. sc[nt][0/1]: token g, rows 2c/2c+1;
+      // sc[nt][2/3]: token g+8, same rows.
+      float bmax[NT][2];
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int lim = limit[nt][e];
+          const float s0 = (tok0 + g <= lim) ? sc[nt][e] * p.scale_log2 : -INFINITY;
+          const float s1 = (tok0 + g + 8 <= lim) ? sc[nt][e + 2] * p.scale_log2 : -INFINITY;
+          sc[nt][e] = s0;
+          sc[nt][e + 2] = s1;
+          bmax[nt][e] = fmaxf(s0, s1);
+        }
+#pragma unroll
+      for (int off = 4; off < 32; off <<= 1)
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+          for (int e = 0; e < 2; ++e)
+            bmax[nt][e] = fmaxf(bmax[nt][e], __shfl_xor_sync(0xffffffffu, bmax[nt][e], off));
+
+      // Online softmax update. P enters the MMA as a sum of two bf16 parts,
+      // p = hi + lo (hi = bf16(p), lo = bf16(p - hi)), so the weights carry
+      // about 16 mantissa bits: a single bf16 rounding of p (2^-9 relative)
+      // can cost more than the output tolerance when a short context's
+      // weighted V rows cancel.
+      uint32_t pb[NT][2], pl[NT][2];
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        float alpha[2], pr[4];
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const float m_new = fmaxf(m_run[nt][e], bmax[nt][e]);
+          const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
+          alpha[e] = fast_exp2(m_run[nt][e] - m_use);
+          m_run[nt][e] = m_new;
+          pr[e] = fast_exp2(sc[nt][e] - m_use);
+          pr[e + 2] = fast_exp2(sc[nt][e + 2] - m_use);
+        }
+        const uint32_t x0 = pack_bf16x2(pr[0], pr[1]);  // token g,   rows 2c, 2c+1
+        const uint32_t x1 = pack_bf16x2(pr[2], pr[3]);  // token g+8, rows 2c, 2c+1
+        const uint32_t y0 = pack_bf16x2(pr[0] - bf16_lo(x0), pr[1] - bf16_hi(x0));
+        const uint32_t y1 = pack_bf16x2(pr[2] - bf16_lo(x1), pr[3] - bf16_hi(x1));
+        l_run[nt][0] = alpha[0] * l_run[nt][0] + (pr[0] + pr[2]);
+        l_run[nt][1] = alpha[1] * l_run[nt][1] + (pr[1] + pr[3]);
+        pb[nt][0] = movmatrix_trans(x0);  // P^T (hi): tokens 2c, 2c+1 of row g
+        pb[nt][1] = movmatrix_trans(x1);  // P^T (hi): tokens 8+2c, 9+2c of row g
+        pl[nt][0] = movmatrix_trans(y0);  // P^T (lo)
+        pl[nt][1] = movmatrix_trans(y1);
+#pragma unroll
+        for (int mt = 0; mt < 8; ++mt) {
+          o[mt][nt][0] *= alpha[0];
+          o[mt][nt][1] *= alpha[1];
+          o[mt][nt][2] *= alpha[0];
+          o[mt][nt][3] *= alpha[1];
+        }
+      }
+
+      // O^T (128 dims x 8*NT rows) += V^T (128 x 16 tokens) . P^T (16 x 8*NT)
+#pragma unroll
+      for (int mt = 0; mt < 8; ++mt) {
+        uint32_t a[4];
+        ldsm_x4_trans(vt + tile_off(v_tok, 2 * mt + v_chunk), a[0], a[1], a[2], a[3]);
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+          mma_bf16_16816(o[mt][nt], a, pb[nt][0], pb[nt][1]);
+          mma_bf16_16816(o[mt][nt], a, pl[nt][0], pl[nt][1]);
+        }
+      }
+
+      // Hand the stage back to the producer. Generic-proxy writes made above
+      // must be ordered before the next TMA write into this stage.
+      if (patched) fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_empty + 8 * s);
+    }
+
+    // Row sums were kept per thread (over its tokens); reduce across lanes.
+#pragma unroll
+    for (int off = 4; off < 32; off <<= 1)
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) l_run[nt][e] += __shfl_xor_sync(0xffffffffu, l_run[nt][e], off);
+  }
+  __syncthreads();
+
+  if (s_flag[2]) {
+    // A wait gave up: let every load already issued land (bounded) before the
+    // CTA leaves, and write nothing.
+    if (threadIdx.x == 0) {
+      const int issued = s_flag[1];
+      for (int j = max(0, issued - kStages); j < issued; ++j)
+        (void)mbar_wait(bar_full + 8 * (j % kStages), (j / kStages) & 1);
+    }
+    __syncthreads();
+    return;
+  }
+
+  // Every stage has been consumed; the ring now holds the cross-warp combine.
+  float* cbuf = reinterpret_cast<float*>(sbase + MmaSmem::stages);
+  if (warp < kConsumerWarps) {
+    float* mine = cbuf + warp * kRowSlots * kCombineStride;
+#pragma unroll
+    for (int mt = 0; mt < 8; ++mt)
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        const int r = nt * 8 + 2 * c, d = mt * 16 + g;
+        mine[r * kCombineStride + d] = o[mt][nt][0];
+        mine[(r + 1) * kCombineStride + d] = o[mt][nt][1];
+        mine[r * kCombineStride + d + 8] = o[mt][nt][2];
+        mine[(r + 1) * kCombineStride + d + 8] = o[mt][nt][3];
+      }
+    if (g == 0) {
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          s_m[warp * kRowSlots + nt * 8 + 2 * c + e] = m_run[nt][e];
+          s_l[warp * kRowSlots + nt * 8 + 2 * c + e] = l_run[nt][e];
+        }
+    }
+  }
+  __syncthreads();
+  split_epilogue<uint16_t>(p, w, cbuf, s_m, s_l, kConsumerWarps, s_flag);
+}
+
+size_t mma_smem_bytes() { return MmaSmem::alloc; }
+
+template <int NT>
+static cudaError_t launch_nt(const CUtensorMap& tk, const CUtensorMap& tv, const AttnParams& p,
+                             dim3 grid, cudaStream_t stream) {
+  static int configured[64] = {0};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev >= 0 && dev < 64 && !configured[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(attn_mma_kernel<NT>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         MmaSmem::alloc);
+    if (e != cudaSuccess) return e;
+    configured[dev] = 1;
+  }
+  attn_mma_kernel<NT><<<grid, kMmaThreads, MmaSmem::alloc, stream>>>(tk, tv, p);
+  return cudaGetLastError();
+}
+
+// Host entry: NT = 1 covers up to 8 query rows per (sequence, KV head),
+// NT = 2 up to 16 (more rows use several row groups).
+cudaError_t launch_attn_mma(const CUtensorMap& tk, const CUtensorMap& tv, const AttnParams& p,
+                            dim3 grid, cudaStream_t stream) {
+  return p.rows > 8 ? launch_nt<2>(tk, tv, p, grid, stream) : launch_nt<1>(tk, tv, p, grid, stream);
+}
+
+}  // namespace pa

@@ -1,0 +1,365 @@
+// Host side of libpa: argument checks, workspace layout, TMA descriptors,
+// launches, plus the cache-write and validation kernels. See include/pa.h for
+// the contract of every entry point.
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include <cudaTypedefs.h>
+
+#include "pa_device.cuh"
+
+namespace pa {
+cudaError_t launch_attn_mma(const CUtensorMap& tk, const CUtensorMap& tv, const AttnParams& p,
+                            dim3 grid, cudaStream_t stream);
+cudaError_t launch_attn_simt(const AttnParams& p, bool bf16, dim3 grid, cudaStream_t stream);
+}  // namespace pa
+
+namespace {
+
+using namespace pa;
+
+thread_local int g_last_cuda_error = 0;
+
+pa_status cuda_fail(cudaError_t e) {
+  g_last_cuda_error = static_cast<int>(e);
+  return PA_ERR_CUDA;
+}
+
+bool aligned16(const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u) == 0; }
+
+size_t elem_size(int32_t dtype) { return dtype == PA_DTYPE_F32 ? 4 : 2; }
+
+pa_status check_cache(const pa_cache* c) {
+  if (!c || !c->k || !c->v) return PA_ERR_INVALID_ARG;
+  if (c->dtype != PA_DTYPE_F32 && c->dtype != PA_DTYPE_BF16) return PA_ERR_UNSUPPORTED;
+  if (c->head_dim != kHeadDim || c->block_size != kBlockSize) return PA_ERR_UNSUPPORTED;
+  if (c->kv_heads <= 0 || c->num_blocks <= 0) return PA_ERR_INVALID_ARG;
+  if (c->kv_heads > 65535) return PA_ERR_UNSUPPORTED;
+  // Slot and TMA row coordinates are int32: num_blocks * 16 must fit.
+  if (int64_t(c->num_blocks) * kBlockSize > INT32_MAX) return PA_ERR_UNSUPPORTED;
+  if (!aligned16(c->k) || !aligned16(c->v)) return PA_ERR_INVALID_ARG;
+  return PA_OK;
+}
+
+int32_t split_of(const pa_options* o) {
+  return (o && o->split_tokens > 0) ? o->split_tokens : PA_DEFAULT_SPLIT_TOKENS;
+}
+
+// Workspace: [status word | counters | lse partials | o partials], each
+// region 256-byte aligned. Row groups are counted for the 8-row CUDA-core
+// kernel, an upper bound for the 16-row tensor-core kernel.
+struct WsLayout {
+  size_t counters, lse, o, total;
+  int32_t max_splits;
+};
+
+size_t round256(size_t x) { return (x + 255) & ~size_t(255); }
+
+bool ws_layout(int32_t batch, int32_t nq, int32_t q_heads, int32_t kv_heads, int32_t max_ctx,
+               int32_t split, WsLayout* out) {
+  if (batch < 0 || nq < 1 || q_heads <= 0 || kv_heads <= 0 || q_heads % kv_heads) return false;
+  if (max_ctx < 0 || split <= 0) return false;
+  const int64_t rows = int64_t(nq) * (q_heads / kv_heads);
+  const int64_t groups = (rows + 7) / 8;
+  const int64_t splits = std::max<int64_t>(1, (int64_t(max_ctx) + split - 1) / split);
+  const int64_t units = int64_t(batch) * kv_heads * groups;
+  WsLayout L;
+  L.max_splits = static_cast<int32_t>(splits);
+  L.counters = 256;
+  L.lse = L.counters + round256(size_t(units) * 4);
+  L.o = L.lse + round256(size_t(units * splits * kRowSlots) * 4);
+  L.total = L.o + round256(size_t(units * splits * kRowSlots) * kHeadDim * 4);
+  *out = L;
+  return true;
+}
+
+using EncodeTiledFn = PFN_cuTensorMapEncodeTiled_v12000;
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(ptr);
+  });
+  return fn;
+}
+
+// A 3-D view [kv_heads][num_blocks * 16][128] of one bf16 pool; boxes of
+// 16 token rows x 64 dims, 128-byte swizzled, zeros outside the tensor.
+bool make_pool_map(CUtensorMap* map, void* pool, int32_t kv_heads, int32_t num_blocks) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {cuuint64_t(kHeadDim), cuuint64_t(num_blocks) * kBlockSize,
+                        cuuint64_t(kv_heads)};
+  cuuint64_t strides[2] = {cuuint64_t(kHeadDim) * 2, cuuint64_t(num_blocks) * kBlockSize * kHeadDim * 2};
+  cuuint32_t box[3] = {64, 16, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, pool, dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// ---------------------------------------------------------------------------
+// Cache write: one thread per 16-byte chunk of each new K or V row.
+
+__global__ void cache_write_kernel(uint4* __restrict__ kc, uint4* __restrict__ vc,
+                                   const uint4* __restrict__ kn, const uint4* __restrict__ vn,
+                                   const int32_t* __restrict__ slots, int32_t n, int32_t kv_heads,
+                                   int32_t num_blocks, int32_t chunks_per_row) {
+  const int64_t total = int64_t(n) * kv_heads * 2 * chunks_per_row;
+  const int64_t num_slots = int64_t(num_blocks) * kBlockSize;
+  for (int64_t idx = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; idx < total;
+       idx += int64_t(gridDim.x) * blockDim.x) {
+    const int c = int(idx % chunks_per_row);
+    int64_t rest = idx / chunks_per_row;
+    const int is_v = int(rest & 1);
+    rest >>= 1;
+    const int h = int(rest % kv_heads);
+    const int64_t i = rest / kv_heads;
+    const int64_t slot = __ldg(slots + i);
+    if (slot < 0 || slot >= num_slots) continue;
+    const int64_t src = (i * kv_heads + h) * chunks_per_row + c;
+    const int64_t dst = ((int64_t(h) * num_blocks + slot / kBlockSize) * kBlockSize + slot % kBlockSize) *
+                            chunks_per_row + c;
+    if (is_v)
+      vc[dst] = __ldg(vn + src);
+    else
+      kc[dst] = __ldg(kn + src);
+  }
+}
+
+// Validation: one CTA per sequence; counts into a 4-word report.
+__global__ void validate_kernel(const int32_t* __restrict__ tables, int32_t mbps,
+                                const int32_t* __restrict__ lens, int32_t max_ctx, int32_t num_blocks,
+                                const int32_t* __restrict__ slots, int32_t nq, uint32_t* report) {
+  const int b = blockIdx.x;
+  int L = lens[b];
+  const int cap = min(max_ctx, mbps * kBlockSize);
+  const bool bad_len = L < 0 || L > cap || (nq > 1 && L < nq);
+  if (threadIdx.x == 0 && bad_len) {
+    atomicAdd(report + 1, 1u);
+    atomicOr(report, PA_FLAG_BAD_LENGTH);
+  }
+  L = max(0, min(L, cap));
+  const int nblk = (L + kBlockSize - 1) / kBlockSize;
+  for (int j = threadIdx.x; j < nblk; j += blockDim.x) {
+    const int id = tables[int64_t(b) * mbps + j];
+    if (id < 0 || id >= num_blocks) {
+      atomicAdd(report + 2, 1u);
+      atomicOr(report, PA_FLAG_BAD_BLOCK);
+    }
+  }
+  if (!slots) return;
+  for (int i = threadIdx.x; i < nq; i += blockDim.x) {
+    const int s = slots[int64_t(b) * nq + i];
+    const int pos = L - nq + i;
+    int expect = -1;
+    if (pos >= 0) {
+      const int id = tables[int64_t(b) * mbps + pos / kBlockSize];
+      expect = (id >= 0 && id < num_blocks) ? id * kBlockSize + pos % kBlockSize : -2;
+    }
+    const bool in_range = s >= -1 && int64_t(s) < int64_t(num_blocks) * kBlockSize;
+    if (!in_range || s != expect) {
+      atomicAdd(report + 3, 1u);
+      atomicOr(report, PA_FLAG_BAD_SLOT);
+    }
+  }
+}
+
+// Shared by pa_decode and pa_verify.
+pa_status attend(const pa_cache* cache, const void* q, void* out, const void* k_new,
+                 const void* v_new, const int32_t* slots, int32_t nq, const int32_t* tables,
+                 int32_t mbps, const int32_t* lens, int32_t batch, int32_t q_heads,
+                 int32_t max_ctx, float scale, void* ws, size_t ws_bytes, const pa_options* opts,
+                 void* stream_ptr) {
+  pa_status st = check_cache(cache);
+  if (st != PA_OK) return st;
+  if (batch < 0 || max_ctx < 0 || nq < 1 || q_heads <= 0) return PA_ERR_INVALID_ARG;
+  if (q_heads % cache->kv_heads) return PA_ERR_INVALID_ARG;
+  if (!std::isfinite(scale)) return PA_ERR_INVALID_ARG;
+  const int32_t split = split_of(opts);
+  if (split % kBlockSize || split > kMaxSplitTokens) return PA_ERR_UNSUPPORTED;
+  const int32_t kernel = opts ? opts->kernel : PA_KERNEL_AUTO;
+  if (kernel < PA_KERNEL_AUTO || kernel > PA_KERNEL_SIMT) return PA_ERR_UNSUPPORTED;
+  const bool bf16 = cache->dtype == PA_DTYPE_BF16;
+  const bool use_mma = (kernel == PA_KERNEL_MMA) || (kernel == PA_KERNEL_AUTO && bf16);
+  if (use_mma && !bf16) return PA_ERR_UNSUPPORTED;
+  if (batch == 0) return PA_OK;
+  if (!q || !out || !tables || !lens || !aligned16(q) || !aligned16(out)) return PA_ERR_INVALID_ARG;
+  if (mbps <= 0 || int64_t(max_ctx) > int64_t(mbps) * kBlockSize) return PA_ERR_INVALID_ARG;
+  const bool fused = (k_new != nullptr);
+  if (fused && (!v_new || !slots || !aligned16(k_new) || !aligned16(v_new))) return PA_ERR_INVALID_ARG;
+
+  WsLayout L;
+  if (!ws_layout(batch, nq, q_heads, cache->kv_heads, max_ctx, split, &L)) return PA_ERR_INVALID_ARG;
+  if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u) || ws_bytes < L.total) return PA_ERR_WORKSPACE;
+
+  AttnParams p;
+  std::memset(&p, 0, sizeof p);
+  p.k_cache = cache->k;
+  p.v_cache = cache->v;
+  p.k_cache_w = cache->k;
+  p.v_cache_w = cache->v;
+  p.q = q;
+  p.out = out;
+  p.k_new = k_new;
+  p.v_new = v_new;
+  p.slot_mapping = slots;
+  p.block_tables = tables;
+  p.context_lens = lens;
+  uint8_t* wsb = static_cast<uint8_t*>(ws);
+  p.status = reinterpret_cast<uint32_t*>(wsb);
+  p.counters = reinterpret_cast<int32_t*>(wsb + L.counters);
+  p.part_lse = reinterpret_cast<float*>(wsb + L.lse);
+  p.part_o = reinterpret_cast<float*>(wsb + L.o);
+  p.kv_heads = cache->kv_heads;
+  p.num_blocks = cache->num_blocks;
+  p.mbps = mbps;
+  p.batch = batch;
+  p.q_heads = q_heads;
+  p.group = q_heads / cache->kv_heads;
+  p.num_queries = nq;
+  p.rows = nq * p.group;
+  p.rows_per_cta = use_mma ? 16 : 8;
+  p.row_groups = (p.rows + p.rows_per_cta - 1) / p.rows_per_cta;
+  p.max_context_len = max_ctx;
+  p.split_tokens = split;
+  p.max_splits = L.max_splits;
+  p.fused_write = fused ? 1 : 0;
+  p.scale_log2 = scale * 1.4426950408889634f;
+
+  const int64_t gz = int64_t(batch) * p.row_groups;
+  if (gz > 65535) return PA_ERR_UNSUPPORTED;
+  const dim3 grid(unsigned(L.max_splits), unsigned(cache->kv_heads), unsigned(gz));
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
+
+  cudaError_t e;
+  if (use_mma) {
+    CUtensorMap tk, tv;
+    if (!make_pool_map(&tk, cache->k, cache->kv_heads, cache->num_blocks) ||
+        !make_pool_map(&tv, cache->v, cache->kv_heads, cache->num_blocks))
+      return cuda_fail(cudaErrorInvalidValue);
+    e = launch_attn_mma(tk, tv, p, grid, stream);
+  } else {
+    e = launch_attn_simt(p, bf16, grid, stream);
+  }
+  if (e != cudaSuccess) return cuda_fail(e);
+  return PA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+pa_status pa_cache_write(const pa_cache* cache, const void* k_new, const void* v_new,
+                         const int32_t* slot_mapping, int32_t num_tokens, void* stream) {
+  pa_status st = check_cache(cache);
+  if (st != PA_OK) return st;
+  if (num_tokens < 0) return PA_ERR_INVALID_ARG;
+  if (num_tokens == 0) return PA_OK;
+  if (!k_new || !v_new || !slot_mapping || !aligned16(k_new) || !aligned16(v_new))
+    return PA_ERR_INVALID_ARG;
+  const int32_t cpr = int32_t(kHeadDim * elem_size(cache->dtype) / 16);
+  const int64_t total = int64_t(num_tokens) * cache->kv_heads * 2 * cpr;
+  const int threads = 256;
+  const int64_t blocks = std::min<int64_t>((total + threads - 1) / threads, 152 * 16);
+  cache_write_kernel<<<unsigned(blocks), threads, 0, static_cast<cudaStream_t>(stream)>>>(
+      static_cast<uint4*>(cache->k), static_cast<uint4*>(cache->v), static_cast<const uint4*>(k_new),
+      static_cast<const uint4*>(v_new), slot_mapping, num_tokens, cache->kv_heads, cache->num_blocks,
+      cpr);
+  const cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? PA_OK : cuda_fail(e);
+}
+
+size_t pa_workspace_size(int32_t batch, int32_t num_queries, int32_t q_heads, int32_t kv_heads,
+                         int32_t head_dim, int32_t max_context_len, const pa_options* opts) {
+  if (head_dim != kHeadDim) return 0;
+  WsLayout L;
+  if (!ws_layout(batch, num_queries, q_heads, kv_heads, max_context_len, split_of(opts), &L)) return 0;
+  return L.total;
+}
+
+pa_status pa_workspace_init(void* workspace, size_t bytes, void* stream) {
+  if (!workspace) return PA_ERR_INVALID_ARG;
+  const cudaError_t e = cudaMemsetAsync(workspace, 0, bytes, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? PA_OK : cuda_fail(e);
+}
+
+pa_status pa_workspace_status(void* workspace, uint32_t* host_flags, void* stream) {
+  if (!workspace || !host_flags) return PA_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint32_t v = 0;
+  cudaError_t e = cudaMemcpyAsync(&v, workspace, sizeof v, cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e == cudaSuccess) e = cudaMemsetAsync(workspace, 0, sizeof v, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return cuda_fail(e);
+  *host_flags = v;
+  return PA_OK;
+}
+
+pa_status pa_decode(const pa_cache* cache, const void* q, void* out, const int32_t* block_tables,
+                    int32_t max_blocks_per_seq, const int32_t* context_lens, int32_t batch,
+                    int32_t q_heads, int32_t max_context_len, float scale, void* workspace,
+                    size_t workspace_bytes, const pa_options* opts, void* stream) {
+  return attend(cache, q, out, nullptr, nullptr, nullptr, 1, block_tables, max_blocks_per_seq,
+                context_lens, batch, q_heads, max_context_len, scale, workspace, workspace_bytes, opts,
+                stream);
+}
+
+pa_status pa_verify(const pa_cache* cache, const void* q, void* out, const void* k_new,
+                    const void* v_new, const int32_t* slot_mapping, int32_t num_queries,
+                    const int32_t* block_tables, int32_t max_blocks_per_seq,
+                    const int32_t* context_lens, int32_t batch, int32_t q_heads,
+                    int32_t max_context_len, float scale, void* workspace, size_t workspace_bytes,
+                    const pa_options* opts, void* stream) {
+  if (num_queries < 1) return PA_ERR_INVALID_ARG;
+  if (batch > 0 && (!k_new || !v_new || !slot_mapping)) return PA_ERR_INVALID_ARG;
+  return attend(cache, q, out, k_new, v_new, slot_mapping, num_queries, block_tables,
+                max_blocks_per_seq, context_lens, batch, q_heads, max_context_len, scale, workspace,
+                workspace_bytes, opts, stream);
+}
+
+pa_status pa_validate(const pa_cache* cache, const int32_t* block_tables, int32_t max_blocks_per_seq,
+                      const int32_t* context_lens, int32_t batch, int32_t max_context_len,
+                      const int32_t* slot_mapping, int32_t num_queries, uint32_t* report,
+                      void* stream) {
+  pa_status st = check_cache(cache);
+  if (st != PA_OK) return st;
+  if (!report || batch < 0 || num_queries < 1 || max_blocks_per_seq <= 0 || max_context_len < 0)
+    return PA_ERR_INVALID_ARG;
+  if (batch > 0 && (!block_tables || !context_lens)) return PA_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaMemsetAsync(report, 0, PA_VALIDATE_WORDS * sizeof(uint32_t), s);
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (batch == 0) return PA_OK;
+  validate_kernel<<<unsigned(batch), 128, 0, s>>>(block_tables, max_blocks_per_seq, context_lens,
+                                                   max_context_len, cache->num_blocks, slot_mapping,
+                                                   num_queries, report);
+  e = cudaGetLastError();
+  return e == cudaSuccess ? PA_OK : cuda_fail(e);
+}
+
+const char* pa_status_string(pa_status status) {
+  switch (status) {
+    case PA_OK: return "PA_OK";
+    case PA_ERR_INVALID_ARG: return "PA_ERR_INVALID_ARG";
+    case PA_ERR_UNSUPPORTED: return "PA_ERR_UNSUPPORTED";
+    case PA_ERR_WORKSPACE: return "PA_ERR_WORKSPACE";
+    case PA_ERR_CUDA: return "PA_ERR_CUDA";
+  }
+  return "PA_ERR_UNKNOWN";
+}
+
+int pa_last_cuda_error(void) { return g_last_cuda_error; }
+
+int pa_version(void) { return 100; }
+
+}  // extern "C"

@@ -1,0 +1,72 @@
+"""pa_validate and the in-kernel range checks on bad device indices (GPU).
+
+Bad indices are safe by construction: a bad block id becomes a TMA coordinate
+outside the tensor (zeros are read) or is skipped on the CUDA-core path; a
+slot outside the pool is skipped; a length above the limits is clamped.
+"""
+
+import numpy as np
+import pytest
+
+from paged_kv_decode_pa_gb300 import _lib, inputs
+
+pytestmark = pytest.mark.gpu
+
+
+def _dev(w):
+    import paged_kv_decode_pa_gb300 as pa
+
+    return {k: pa.to_torch(getattr(w, k)) for k in
+            ("k_cache", "v_cache", "q", "block_tables", "context_lens", "slot_mapping")}
+
+
+def test_validate_counts_bad_entries():
+    import torch
+
+    import paged_kv_decode_pa_gb300 as pa
+
+    w = inputs.custom(batch=4, q_heads=12, kv_heads=2, context_lens=(5, 40, 70, 16), num_blocks=64,
+                      dtype="bf16", seed=41)
+    d = _dev(w)
+    rep = pa.pa_validate(d["k_cache"], d["v_cache"], d["block_tables"], d["context_lens"],
+                         w.max_context_len, d["slot_mapping"], 1)
+    torch.cuda.synchronize()
+    assert rep.cpu().tolist() == [0, 0, 0, 0]
+
+    tables = w.block_tables.copy()
+    tables[1, 1] = 64          # one past the pool
+    tables[2, 0] = -5
+    lens = w.context_lens.copy()
+    lens[3] = 10 ** 6          # beyond max_context_len
+    slots = w.slot_mapping.copy()
+    slots[0] = slots[0] + 1    # not the slot of its position
+    rep = pa.pa_validate(d["k_cache"], d["v_cache"], pa.to_torch(tables), pa.to_torch(lens),
+                         w.max_context_len, pa.to_torch(slots), 1)
+    torch.cuda.synchronize()
+    flags, bad_len, bad_blk, bad_slot = rep.cpu().tolist()
+    assert bad_len == 1 and bad_blk == 2 and bad_slot >= 1
+    assert flags == _lib.PA_FLAG_BAD_LENGTH | _lib.PA_FLAG_BAD_BLOCK | _lib.PA_FLAG_BAD_SLOT
+
+
+@pytest.mark.parametrize("kernel", ["mma", "simt"])
+def test_decode_flags_bad_ids_and_reads_nothing_outside(kernel):
+    import torch
+
+    import paged_kv_decode_pa_gb300 as pa
+
+    w = inputs.custom(batch=3, q_heads=12, kv_heads=2, context_lens=(40, 40, 40), num_blocks=16,
+                      dtype="bf16", seed=43)
+    tables = w.block_tables.copy()
+    tables[1, 1] = 1 << 30
+    d = _dev(w)
+    ws = pa.new_workspace(3, 1, 12, 2, 40)
+    out = pa.pa_decode(d["k_cache"], d["v_cache"], d["q"], pa.to_torch(tables), d["context_lens"], 40,
+                       w.scale, ws, kernel=kernel)
+    torch.cuda.synchronize()
+    assert pa.pa_workspace_status(ws) & _lib.PA_FLAG_BAD_BLOCK
+    good = pa.pa_decode(d["k_cache"], d["v_cache"], d["q"], d["block_tables"], d["context_lens"], 40,
+                        w.scale, ws, kernel=kernel)
+    torch.cuda.synchronize()
+    assert pa.pa_workspace_status(ws) == 0
+    o, g = pa.to_numpy(out), pa.to_numpy(good)
+    assert np.array_equal(o[[0, 2]], g[[0, 2]]), "a bad id in one sequence changed another"

@@ -227,6 +227,36 @@ pa_status pa_validate(const pa_cache *cache, const int32_t *d_block_tables,
                       int32_t max_context_len, const int32_t *d_slot_mapping,
                       int32_t num_queries, uint32_t *d_report, void *stream);
 
+/*
+ * pa_decode_noalloc: pa_decode for callers that cannot allocate device memory
+ * at the point of the call, for example a plugin running inside a host program
+ * that owns every device allocation itself, or code that must not grow the
+ * device's memory footprint once it is running. The pages have no counterpart
+ * to this call; it exists for those callers only.
+ *
+ * Arguments and results are those of pa_decode without the workspace: the
+ * split partials, arrival counters and status word live instead in one
+ * library-owned device array of PA_NOALLOC_SCRATCH_BYTES, which every GPU that
+ * loads the library holds until the process exits. The call itself allocates
+ * and frees nothing.
+ *  - Sizes whose pa_workspace_size() exceeds PA_NOALLOC_SCRATCH_BYTES return
+ *    PA_ERR_WORKSPACE before anything is launched.
+ *  - The first call on a device looks up that device's address of the array
+ *    (with that device current); make that first call before any stream
+ *    capture on the device.
+ *  - Every call reuses the same array and clears the parts that must start at
+ *    zero. Calls whose work overlaps on the GPU (different streams, or
+ *    different host threads on one device) race on it: serialise them.
+ *  - The status word is not readable through this call; use pa_validate to
+ *    check device-resident indices.
+ */
+#define PA_NOALLOC_SCRATCH_BYTES (16u << 20)
+pa_status pa_decode_noalloc(const pa_cache *cache, const void *d_q, void *d_out,
+                            const int32_t *d_block_tables, int32_t max_blocks_per_seq,
+                            const int32_t *d_context_lens, int32_t batch, int32_t q_heads,
+                            int32_t max_context_len, float scale, const pa_options *opts,
+                            void *stream);
+
 /* Human-readable name of a status. */
 const char *pa_status_string(pa_status status);
 

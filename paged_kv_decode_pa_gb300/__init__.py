@@ -7,10 +7,12 @@ in include/pa.h). This package builds it (``build``), binds it with ctypes
 algorithmic byte counts used for the roofline.
 """
 
-from .api import (make_cache, new_workspace, pa_cache_write, pa_decode, pa_status_string,  # noqa: F401
+from .api import (make_cache, new_workspace, pa_cache_write, pa_decode, pa_decode_noalloc,  # noqa: F401
+                  pa_status_string,
                   pa_validate, pa_verify, pa_version, pa_workspace_init, pa_workspace_size,
                   pa_workspace_status, to_numpy, to_torch)
 
-__all__ = ["make_cache", "new_workspace", "pa_cache_write", "pa_decode", "pa_verify", "pa_validate",
+__all__ = ["make_cache", "new_workspace", "pa_cache_write", "pa_decode", "pa_decode_noalloc", "pa_verify",
+           "pa_validate",
            "pa_workspace_size", "pa_workspace_init", "pa_workspace_status", "pa_status_string",
            "pa_version", "to_torch", "to_numpy"]

@@ -31,11 +31,12 @@ PA_FLAG_TIMEOUT = 0x8
 
 PA_DEFAULT_SPLIT_TOKENS = 512
 PA_VALIDATE_WORDS = 4
+PA_NOALLOC_SCRATCH_BYTES = 16 << 20
 
 # Every symbol include/pa.h declares.
 EXPORTED = ("pa_cache_write", "pa_workspace_size", "pa_workspace_init", "pa_workspace_status",
-            "pa_decode", "pa_verify", "pa_validate", "pa_status_string", "pa_last_cuda_error",
-            "pa_version")
+            "pa_decode", "pa_verify", "pa_validate", "pa_decode_noalloc", "pa_status_string",
+            "pa_last_cuda_error", "pa_version")
 
 
 class PaCache(ctypes.Structure):
@@ -90,6 +91,8 @@ def load(path: Path | None = None):
         "pa_verify": (ctypes.c_int, [cache_p, vp, vp, vp, vp, vp, i32, vp, i32, vp, i32, i32, i32,
                                      ctypes.c_float, vp, ctypes.c_size_t, opts_p, vp]),
         "pa_validate": (ctypes.c_int, [cache_p, vp, i32, vp, i32, i32, vp, i32, vp, vp]),
+        "pa_decode_noalloc": (ctypes.c_int, [cache_p, vp, vp, vp, i32, vp, i32, i32, i32,
+                                             ctypes.c_float, opts_p, vp]),
         "pa_status_string": (ctypes.c_char_p, [ctypes.c_int]),
         "pa_last_cuda_error": (ctypes.c_int, []),
         "pa_version": (ctypes.c_int, []),

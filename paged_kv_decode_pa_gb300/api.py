@@ -118,6 +118,27 @@ def pa_decode(k_cache, v_cache, q, block_tables, context_lens, max_context_len: 
     return out
 
 
+def pa_decode_noalloc(k_cache, v_cache, q, block_tables, context_lens, max_context_len: int,
+                      scale: float, out=None, split_tokens: int = 0, kernel: str = "auto", stream=None):
+    """pa_decode without a caller workspace, for callers that cannot allocate device memory.
+
+    The scratch is a fixed library-owned device array (PA_NOALLOC_SCRATCH_BYTES);
+    overlapping calls on the GPU race on it. Only ``out`` may be allocated here,
+    and only when it is not passed.
+    """
+    cache = make_cache(k_cache, v_cache)
+    _need(q.dim() == 3 and q.dtype == k_cache.dtype and q.is_contiguous(), "q must be [batch, q_heads, head_dim]")
+    batch, q_heads, _ = q.shape
+    mbps = _tables(block_tables, context_lens, batch)
+    if out is None:
+        out = torch.empty_like(q)
+    opts = _options(split_tokens, kernel)
+    L.check("pa_decode_noalloc", L.load().pa_decode_noalloc(
+        ctypes.byref(cache), _vp(q), _vp(out), _vp(block_tables), mbps, _vp(context_lens), batch,
+        q_heads, int(max_context_len), float(scale), ctypes.byref(opts), _stream(stream)))
+    return out
+
+
 def pa_verify(k_cache, v_cache, q, k_new, v_new, slot_mapping, block_tables, context_lens,
               max_context_len: int, scale: float, workspace, out=None, split_tokens: int = 0,
               kernel: str = "auto", stream=None):

@@ -256,6 +256,18 @@ pa_status attend(const pa_cache* cache, const void* q, void* out, const void* k_
 
 }  // namespace
 
+namespace pa {
+// Bytes at the start of a workspace that must be zero when a call starts
+// (status word and arrival counters); 0 if the sizes are invalid.
+size_t workspace_zero_prefix(int32_t batch, int32_t nq, int32_t q_heads, int32_t kv_heads,
+                             int32_t max_ctx, int32_t split) {
+  WsLayout L;
+  return ws_layout(batch, nq, q_heads, kv_heads, max_ctx, split, &L) ? L.lse : 0;
+}
+
+void record_cuda_error(cudaError_t e) { g_last_cuda_error = static_cast<int>(e); }
+}  // namespace pa
+
 extern "C" {
 
 pa_status pa_cache_write(const pa_cache* cache, const void* k_new, const void* v_new,

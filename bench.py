@@ -9,7 +9,8 @@ verify are measured too and reported under "per_config".
 
 Metric: achieved KV-read bandwidth (algorithmic K+V bytes of every valid token
 per step / step time, GB/s) and microseconds per call. Timing uses CUDA events
-on the launching stream, with L2 flushed (a 256 MiB write) before every timed
+on the launching stream, with L2 flushed (a 256 MiB write, then a 256 MiB read
+that retires the write-backs) before every timed
 step. rank 0 prints one JSON line.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
@@ -50,10 +51,14 @@ def parse_args():
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
-    ap.add_argument("--workload", default="c4", choices=["c2", "c3", "c4"])
+    ap.add_argument("--workload", default="c4", choices=["c2", "c3", "c4", "c5"])
     ap.add_argument("--no-extra", action="store_true", help="skip the per_config measurements")
-    ap.add_argument("--kernel", default="auto", choices=["auto", "mma", "simt"])
+    ap.add_argument("--kernel", default="auto", choices=["auto", "mma", "mma_ldg", "simt"])
+    ap.add_argument("--prefetch", type=int, default=0, help="blocks in flight per warp (mma_ldg kernel)")
+    ap.add_argument("--warps", type=int, default=0, help="warps per split (mma_ldg kernel)")
     ap.add_argument("--split-tokens", type=int, default=0)
+    ap.add_argument("--unfused", action="store_true",
+                    help="time a decode step as two calls, pa_cache_write then pa_decode")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="CPU baseline sample budget")
     return ap.parse_args()
 
@@ -188,9 +193,15 @@ def ncu_traffic(workload: str):
 # GPU arm
 
 class DecodeStep:
-    """Device-resident buffers of one decode workload and the two calls of a step."""
+    """Device-resident buffers of one workload and the call(s) of one step.
 
-    def __init__(self, w, device, split_tokens=0, kernel="auto"):
+    A decode step appends each sequence's new token and attends. By default it
+    is the single fused call (pa_verify with one query per sequence, which is
+    pa_cache_write followed by pa_decode in one launch); with fused=False it is
+    the two calls. A verify workload's step is pa_verify.
+    """
+
+    def __init__(self, w, device, split_tokens=0, kernel="auto", prefetch=0, warps=0, fused=True):
         import paged_kv_decode_pa_gb300 as pa
 
         self.pa = pa
@@ -198,6 +209,8 @@ class DecodeStep:
         self.dev = device
         self.split = split_tokens
         self.kernel = kernel
+        self.prefetch = prefetch
+        self.warps = warps
         self.kc = pa.to_torch(w.k_cache, device)
         self.vc = pa.to_torch(w.v_cache, device)
         self.q = pa.to_torch(w.q, device)
@@ -209,6 +222,9 @@ class DecodeStep:
         self.out = self.q.new_empty(self.q.shape)
         s = w.spec
         self.nq = s.num_queries
+        self.fused = fused or self.nq > 1
+        self.q4 = self.q if self.q.dim() == 4 else self.q.unsqueeze(1)
+        self.out4 = self.out if self.out.dim() == 4 else self.out.unsqueeze(1)
         self.ws = pa.new_workspace(s.batch, self.nq, s.q_heads, s.kv_heads, w.max_context_len, device,
                                    split_tokens)
 
@@ -217,33 +233,67 @@ class DecodeStep:
 
     def attend(self):
         w = self.w
-        if self.nq == 1:
+        if not self.fused:
             self.pa.pa_decode(self.kc, self.vc, self.q, self.tables, self.lens, w.max_context_len, w.scale,
-                              self.ws, out=self.out, split_tokens=self.split, kernel=self.kernel)
+                              self.ws, out=self.out, split_tokens=self.split, kernel=self.kernel,
+                              prefetch=self.prefetch, warps=self.warps)
         else:
-            self.pa.pa_verify(self.kc, self.vc, self.q, self.k_new, self.v_new, self.slots, self.tables,
-                              self.lens, w.max_context_len, w.scale, self.ws, out=self.out,
-                              split_tokens=self.split, kernel=self.kernel)
+            self.pa.pa_verify(self.kc, self.vc, self.q4, self.k_new, self.v_new, self.slots, self.tables,
+                              self.lens, w.max_context_len, w.scale, self.ws, out=self.out4,
+                              split_tokens=self.split, kernel=self.kernel, prefetch=self.prefetch,
+                              warps=self.warps)
+
+    def run(self):
+        """One whole step."""
+        if not self.fused:
+            self.write()
+        self.attend()
 
 
-def time_steps(step: DecodeStep, steps: int, warmup: int, flush, with_write=True):
-    """Per-step CUDA-event times (ms) of the whole step and of the attention call."""
+def make_l2_flush(device):
+    """Return a function that leaves L2 holding nothing the timed step reads.
+
+    It writes a buffer larger than L2, then reads a second one: the read
+    evicts the dirty lines the write left, so their write-back to HBM happens
+    here and not inside the timed region (where it would compete with the
+    kernel's reads).
+    """
     import torch
 
-    def one():
-        if with_write and step.nq == 1:
-            step.write()
-        step.attend()
+    dirty = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
+    clean = torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=device)
+
+    def flush():
+        dirty.fill_(1)
+        clean.sum()
+
+    return flush
+
+
+def gpu_hold(us: float = 150.0):
+    """A short device-side delay before a timed region (outside it), so that
+    the host has enqueued the step before the GPU reaches the start event."""
+    import torch
+
+    sleep = getattr(torch.cuda, "_sleep", None)
+    if sleep is not None:
+        sleep(int(us * 2000))  # cycles at about 2 GHz
+
+
+def time_steps(step: DecodeStep, steps: int, warmup: int, flush):
+    """Per-step CUDA-event times (ms) of the whole step and of its attention call."""
+    import torch
 
     for _ in range(warmup):
         flush()
-        one()
+        step.run()
     torch.cuda.synchronize()
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
     for k in range(steps):
         flush()
+        gpu_hold()
         ev[k][0].record()
-        if with_write and step.nq == 1:
+        if not step.fused:
             step.write()
         ev[k][1].record()
         step.attend()
@@ -271,8 +321,7 @@ def time_e2e(step: DecodeStep, steps: int, warmup: int, flush):
     def one():
         for name, t in host.items():
             dev[name].copy_(t, non_blocking=True)
-        step.write()
-        step.attend()
+        step.run()
         out_host.copy_(step.out, non_blocking=True)
 
     for _ in range(warmup):
@@ -289,19 +338,21 @@ def time_e2e(step: DecodeStep, steps: int, warmup: int, flush):
     return [e[0].elapsed_time(e[1]) for e in ev], h2d, d2h
 
 
-def step_bytes(w):
+def step_bytes(w, fused=True):
     s = w.spec
     eb = accounting.elem_bytes(s.dtype)
-    att = accounting.decode_bytes(w.context_lens, s.q_heads, s.kv_heads, s.head_dim, eb, s.num_queries)
-    write = accounting.cache_write_bytes(len(w.slot_mapping), s.kv_heads, s.head_dim, eb) if s.num_queries == 1 else 0
+    fused_write = fused or s.num_queries > 1
+    att = accounting.decode_bytes(w.context_lens, s.q_heads, s.kv_heads, s.head_dim, eb, s.num_queries,
+                                  fused_write=fused_write)
+    write = 0 if fused_write else accounting.cache_write_bytes(len(w.slot_mapping), s.kv_heads, s.head_dim, eb)
     return att, write
 
 
-def measure_extra(name, device, steps, flush, split, kernel):
+def measure_extra(name, device, steps, flush, split, kernel, prefetch=0, warps=0, fused=True):
     w = inputs.make(name)
-    st = DecodeStep(w, device, split, kernel)
+    st = DecodeStep(w, device, split, kernel, prefetch, warps, fused)
     total, attend = time_steps(st, steps, 3, flush)
-    att, _ = step_bytes(w)
+    att, _ = step_bytes(w, fused)
     us = statistics.mean(attend) * 1e3
     peak, _ = hbm_peak()
     gbs = att["total"] / (us * 1e-6) / 1e9
@@ -311,8 +362,9 @@ def measure_extra(name, device, steps, flush, split, kernel):
            "kv_bytes": att["kv"], "algorithmic_bytes": att["total"],
            "kv_gbs": round(att["kv"] / (us * 1e-6) / 1e9, 1), "achieved_gbs": round(gbs, 1),
            "frac_of_measured_hbm": round(gbs / peak, 3), "frac_of_8tbs": round(gbs / 8000.0, 3),
-           "call": "pa_verify (fused write)" if w.spec.num_queries > 1 else "pa_decode",
-           "l2": "flushed before each call"}
+           "call": ("pa_verify (fused write)" if w.spec.num_queries > 1 else
+                    "pa_verify, one query per sequence (fused append + decode)" if fused else "pa_decode"),
+           "l2": "flushed (write + read) before each call"}
     del st
     return rec
 
@@ -329,13 +381,11 @@ def run_native(args):
     _lib.load()  # fails loudly if the library is missing
     base = inputs.CONFIGS[args.workload]
     w = inputs.generate(base, seed=base.seed + 1000 * rank)
-    step = DecodeStep(w, device, args.split_tokens, args.kernel)
-    flush_buf = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
+    step = DecodeStep(w, device, args.split_tokens, args.kernel, args.prefetch, args.warps,
+                      fused=not args.unfused)
+    flush = make_l2_flush(device)
 
-    def flush():
-        flush_buf.fill_(1)
-
-    att, write = step_bytes(w)
+    att, write = step_bytes(w, step.fused)
     barrier(world)
     torch.cuda.synchronize()
     with ClockSampler(local) as clocks:
@@ -363,7 +413,8 @@ def run_native(args):
     if not args.no_extra and rank == 0:
         for name in ("c2", "c3", "c5"):
             if name != args.workload:
-                extra[name] = measure_extra(name, device, 20, flush, args.split_tokens, args.kernel)
+                extra[name] = measure_extra(name, device, 20, flush, args.split_tokens, args.kernel,
+                                            args.prefetch, args.warps, not args.unfused)
 
     cpu = cpu_baseline(w, args.cpu_seconds) if rank == 0 else None
 
@@ -390,14 +441,21 @@ def run_native(args):
                 "context_tokens": int(w.context_lens.sum()),
                 "split_tokens": args.split_tokens or _lib.PA_DEFAULT_SPLIT_TOKENS,
                 "kernel": args.kernel,
-                "step": "pa_cache_write (one new token per sequence) + pa_decode",
-                "l2": "flushed before every timed step (256 MiB write, outside the timed region)",
+                **({"prefetch": args.prefetch or 1, "warps_per_split": args.warps or 4}
+                   if args.kernel == "mma_ldg" else {}),
+                "step": ("pa_cache_write (one new token per sequence) + pa_decode" if not step.fused
+                         else "pa_verify with one query per sequence: fused append of the new token "
+                              "+ decode, one launch" if s.num_queries == 1
+                         else "pa_verify (fused write of the new tokens + causal attention)"),
+                "l2": "flushed before every timed step (256 MiB write, then 256 MiB read so that the "
+                      "write-backs finish; outside the timed region)",
                 "parallelism": f"replicas x{world} (independent sequences per GPU)",
             },
             "roofline": {
                 "bound": "hbm",
-                "kernel": "pa_decode (attn_mma_kernel)" if s.dtype == "bf16" and args.kernel != "simt"
-                          else "pa_decode (attn_simt_kernel)",
+                "kernel": {"auto": "pa_decode (attn_mma_kernel)", "mma": "pa_decode (attn_mma_kernel)",
+                           "mma_ldg": "pa_decode (attn_ldg_kernel)",
+                           "simt": "pa_decode (attn_simt_kernel)"}[args.kernel],
                 "achieved": round(achieved, 1),
                 "peak": peak,
                 "unit": "GB/s",
@@ -410,8 +468,12 @@ def run_native(args):
             "cpu_baseline": cpu,
             "e2e": {"value": round(kv_total / (e2e_step * 1e-3) / 1e9, 1), "unit": "GB/s",
                     "ms_per_step": round(e2e_step, 5), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                    "path": "pinned host -> device copies, pa_cache_write, pa_decode, device -> host output"},
-            "gpu_launches": 2 * args.steps,
+                    "path": "pinned host -> device copies of the step's inputs, the step's libpa call(s), "
+                            "device -> host copy of the output"},
+            "gpu_launches": ((0 if step.fused else 1) + 1
+                             + (1 if args.kernel == "mma_ldg" and w.max_context_len > (args.split_tokens or
+                                                                                    _lib.PA_DEFAULT_SPLIT_TOKENS) else 0))
+                            * args.steps,
             "clocks": clocks.summary(),
             "wall_s_timed_loop": round(wall, 3),
             "per_config": extra,

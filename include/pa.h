@@ -98,9 +98,12 @@ typedef struct pa_cache {
 
 /* Kernel choice for pa_decode / pa_verify. */
 typedef enum pa_kernel {
-    PA_KERNEL_AUTO = 0, /* bf16: tensor-core kernel; fp32: CUDA-core kernel */
-    PA_KERNEL_MMA = 1,  /* bf16 only: TMA-staged tiles, bf16 tensor-core products, fp32 softmax */
-    PA_KERNEL_SIMT = 2  /* CUDA-core fp32 arithmetic, any dtype (kept for comparison and fp32) */
+    PA_KERNEL_AUTO = 0,    /* bf16: PA_KERNEL_MMA; fp32: PA_KERNEL_SIMT */
+    PA_KERNEL_MMA = 1,     /* bf16 only: a producer warp stages 16-token K/V tiles with TMA
+                              tensor loads; bf16 tensor-core products, fp32 softmax */
+    PA_KERNEL_SIMT = 2,    /* CUDA-core fp32 arithmetic, any dtype (fp32 caches; comparison) */
+    PA_KERNEL_MMA_LDG = 3  /* bf16 only: as PA_KERNEL_MMA but each warp loads its own tiles with
+                              16-byte loads staged through shared memory (kept for comparison) */
 } pa_kernel;
 
 /* Optional tuning for pa_decode / pa_verify; pass NULL for the defaults. */
@@ -110,10 +113,20 @@ typedef struct pa_options {
      * A sequence's result depends only on its own length and this value, never
      * on its batch-mates, so it is bit-identical across batch compositions. */
     int32_t split_tokens;
-    int32_t kernel; /* pa_kernel */
+    int32_t kernel;   /* pa_kernel */
+    /* PA_KERNEL_MMA_LDG only: 16-token blocks each warp keeps in flight, 1 or 2;
+     * 0 = default (PA_DEFAULT_PREFETCH). Values above 1 apply to up to 8 query
+     * rows per (sequence, KV head). */
+    int32_t prefetch;
+    /* PA_KERNEL_MMA_LDG only: warps that share one split, 1, 2 or 4; 0 = default
+     * (PA_DEFAULT_WARPS). */
+    int32_t warps;
 } pa_options;
 
-#define PA_DEFAULT_SPLIT_TOKENS 512
+#define PA_DEFAULT_PREFETCH 1
+#define PA_DEFAULT_WARPS 4
+
+#define PA_DEFAULT_SPLIT_TOKENS 1024
 
 /*
  * pa_cache_write: cache[h, s / 16, s % 16, :] = new[i, h, :] for every token

@@ -23,13 +23,16 @@ PA_DTYPE_BF16 = 1
 PA_KERNEL_AUTO = 0
 PA_KERNEL_MMA = 1
 PA_KERNEL_SIMT = 2
+PA_KERNEL_MMA_LDG = 3
+PA_DEFAULT_PREFETCH = 1
+PA_DEFAULT_WARPS = 4
 
 PA_FLAG_BAD_BLOCK = 0x1
 PA_FLAG_BAD_LENGTH = 0x2
 PA_FLAG_BAD_SLOT = 0x4
 PA_FLAG_TIMEOUT = 0x8
 
-PA_DEFAULT_SPLIT_TOKENS = 512
+PA_DEFAULT_SPLIT_TOKENS = 1024
 PA_VALIDATE_WORDS = 4
 PA_NOALLOC_SCRATCH_BYTES = 16 << 20
 
@@ -46,7 +49,8 @@ class PaCache(ctypes.Structure):
 
 
 class PaOptions(ctypes.Structure):
-    _fields_ = [("split_tokens", ctypes.c_int32), ("kernel", ctypes.c_int32)]
+    _fields_ = [("split_tokens", ctypes.c_int32), ("kernel", ctypes.c_int32),
+                ("prefetch", ctypes.c_int32), ("warps", ctypes.c_int32)]
 
 
 class PaError(RuntimeError):

@@ -32,19 +32,22 @@ def kv_read_bytes(context_lens, kv_heads: int, head_dim: int, elem: int) -> int:
 
 
 def decode_bytes(context_lens, q_heads: int, kv_heads: int, head_dim: int, elem: int,
-                 num_queries: int = 1, block_size: int = 16) -> dict:
-    """Algorithmic bytes of one decode (num_queries = 1) or fused verify call.
+                 num_queries: int = 1, block_size: int = 16, fused_write: bool | None = None) -> dict:
+    """Algorithmic bytes of one decode or fused verify call.
 
-    For verify, the new tokens' K/V are read from the inputs instead of the
-    cache (same count) and written once to the cache.
+    With the fused write (pa_verify, the default whenever num_queries > 1) the
+    new tokens' K/V are read from the inputs instead of the cache (same count)
+    and written once to the cache.
     """
+    if fused_write is None:
+        fused_write = num_queries > 1
     lens = np.asarray(context_lens, dtype=np.int64)
     batch = lens.size
     kv = kv_read_bytes(lens, kv_heads, head_dim, elem)
     qo = 2 * batch * num_queries * q_heads * head_dim * elem          # q read + out written
     tables = int(((lens + block_size - 1) // block_size).sum()) * 4 + batch * 4
     new_writes = 0
-    if num_queries > 1:
+    if fused_write:
         new_writes = batch * num_queries * kv_heads * 2 * head_dim * elem + batch * num_queries * 4
     total = kv + qo + tables + new_writes
     return {"kv": kv, "q_out": qo, "tables": tables, "new_writes": new_writes, "total": total}

@@ -16,7 +16,8 @@ import torch
 from . import _lib as L
 
 _DTYPES = {torch.bfloat16: L.PA_DTYPE_BF16, torch.float32: L.PA_DTYPE_F32}
-_KERNELS = {"auto": L.PA_KERNEL_AUTO, "mma": L.PA_KERNEL_MMA, "simt": L.PA_KERNEL_SIMT}
+_KERNELS = {"auto": L.PA_KERNEL_AUTO, "mma": L.PA_KERNEL_MMA, "simt": L.PA_KERNEL_SIMT,
+            "mma_ldg": L.PA_KERNEL_MMA_LDG}
 
 
 def _vp(t: Optional[torch.Tensor]):
@@ -43,8 +44,8 @@ def make_cache(k_cache: torch.Tensor, v_cache: torch.Tensor) -> L.PaCache:
     return L.PaCache(k_cache.data_ptr(), v_cache.data_ptr(), hkv, nb, bs, d, _DTYPES[k_cache.dtype])
 
 
-def _options(split_tokens: int, kernel: str) -> L.PaOptions:
-    return L.PaOptions(int(split_tokens), _KERNELS[kernel])
+def _options(split_tokens: int, kernel: str, prefetch: int = 0, warps: int = 0) -> L.PaOptions:
+    return L.PaOptions(int(split_tokens), _KERNELS[kernel], int(prefetch), int(warps))
 
 
 def pa_workspace_size(batch: int, num_queries: int, q_heads: int, kv_heads: int,
@@ -102,7 +103,8 @@ def _tables(block_tables, context_lens, batch):
 
 
 def pa_decode(k_cache, v_cache, q, block_tables, context_lens, max_context_len: int, scale: float,
-              workspace, out=None, split_tokens: int = 0, kernel: str = "auto", stream=None):
+              workspace, out=None, split_tokens: int = 0, kernel: str = "auto", stream=None,
+              prefetch: int = 0, warps: int = 0):
     """out[b, hq] = softmax(scale * q[b, hq] . K_b^T) V_b over sequence b's paged context."""
     cache = make_cache(k_cache, v_cache)
     _need(q.dim() == 3 and q.dtype == k_cache.dtype and q.is_contiguous(), "q must be [batch, q_heads, head_dim]")
@@ -110,7 +112,7 @@ def pa_decode(k_cache, v_cache, q, block_tables, context_lens, max_context_len: 
     mbps = _tables(block_tables, context_lens, batch)
     if out is None:
         out = torch.empty_like(q)
-    opts = _options(split_tokens, kernel)
+    opts = _options(split_tokens, kernel, prefetch, warps)
     L.check("pa_decode", L.load().pa_decode(
         ctypes.byref(cache), _vp(q), _vp(out), _vp(block_tables), mbps, _vp(context_lens), batch,
         q_heads, int(max_context_len), float(scale), _vp(workspace),
@@ -141,7 +143,7 @@ def pa_decode_noalloc(k_cache, v_cache, q, block_tables, context_lens, max_conte
 
 def pa_verify(k_cache, v_cache, q, k_new, v_new, slot_mapping, block_tables, context_lens,
               max_context_len: int, scale: float, workspace, out=None, split_tokens: int = 0,
-              kernel: str = "auto", stream=None):
+              kernel: str = "auto", stream=None, prefetch: int = 0, warps: int = 0):
     """Fused speculative verify: write the new K/V, attend causally. q: [batch, nq, q_heads, head_dim]."""
     cache = make_cache(k_cache, v_cache)
     _need(q.dim() == 4 and q.dtype == k_cache.dtype and q.is_contiguous(),
@@ -155,7 +157,7 @@ def pa_verify(k_cache, v_cache, q, k_new, v_new, slot_mapping, block_tables, con
           "new rows must be [batch * num_queries, kv_heads, head_dim] of the cache dtype")
     if out is None:
         out = torch.empty_like(q)
-    opts = _options(split_tokens, kernel)
+    opts = _options(split_tokens, kernel, prefetch, warps)
     L.check("pa_verify", L.load().pa_verify(
         ctypes.byref(cache), _vp(q), _vp(out), _vp(k_new), _vp(v_new), _vp(slot_mapping), nq,
         _vp(block_tables), mbps, _vp(context_lens), batch, q_heads, int(max_context_len),

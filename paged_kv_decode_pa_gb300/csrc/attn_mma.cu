@@ -7,21 +7,21 @@
 // "Then speculative decoding got slower"). The split is a fixed number of
 // tokens, so a sequence's result depends on its own length only.
 //
-// Warp roles (5 warps):
-//   warp 4      producer: one lane walks the split's block-table entries and
+// Warp roles (3 warps):
+//   warp 2      producer: one lane walks the split's block-table entries and
 //               issues TMA tensor loads of each 16-token block, K and V, into a
 //               ring of shared-memory stages (128-byte swizzle, so ldmatrix
 //               reads are bank-conflict free). Each block is a contiguous
 //               16 x 128 tile of the head-major cache ("2. Head-major KV
 //               cache"): no gather, no padded copy.
-//   warps 0..3  consumers: block j goes to warp j % 4. Per block, a warp
+//   warps 0..1  consumers: block j goes to warp j % 2. Per block, a warp
 //               computes S^T = K Q^T (16 tokens x up to 16 rows) with
 //               m16n8k16 bf16 MMAs, masks, runs the fp32 online softmax
 //               (running max and sum, rescaled per block: "3. A Triton
 //               paged-decode kernel"), turns P^T into the B operand in
 //               registers (movmatrix; P split into two bf16 parts), and
 //               accumulates O^T += V^T P^T.
-// Then the four warps' states are combined and the split epilogue writes the
+// Then the two warps' states are combined and the split epilogue writes the
 // output, or a partial plus the log-sum-exp that the last split merges.
 //
 // Masking: a position beyond the sequence (or beyond a verify row's causal
@@ -33,15 +33,18 @@
 // Fused verify: the CTA whose split holds a new token's position writes that
 // token's K/V row to the cache (row group 0 only) and patches the row into its
 // shared-memory tile from the inputs, so no CTA depends on another's write.
-#include "pa_device.cuh"
+#include "mma_tile.cuh"
 
 namespace pa {
 
-constexpr int kStages = 8;              // shared-memory ring depth (blocks in flight per CTA)
-constexpr int kTileBytes = 16 * 128 * 2;  // one 16-token bf16 tile of K or V
-constexpr int kHalfTile = kTileBytes / 2;  // one TMA box: 16 rows x 64 dims, 128-byte swizzled
-constexpr int kStageBytes = 2 * kTileBytes;
-constexpr int kMmaThreads = (kConsumerWarps + 1) * 32;
+// CTA shape, chosen by measurement on GB300 (c2..c5 workloads): two consumer
+// warps and a six-block ring per CTA, four CTAs per SM (three with 16 query
+// rows). The same 24 blocks in flight per SM as three CTAs of four warps with
+// eight stages, but more CTAs, and so more TMA issuers and a finer grid, per SM.
+constexpr int kMmaConsumers = 2;
+constexpr int kStages = 6;                 // shared-memory ring depth (blocks in flight per CTA)
+constexpr int kStageBytes = kBlockBytes;   // one K+V block; each TMA box is 16 rows x 64 dims
+constexpr int kMmaThreads = (kMmaConsumers + 1) * 32;
 
 struct MmaSmem {
   // Offsets from the 1024-byte aligned base.
@@ -49,22 +52,20 @@ struct MmaSmem {
   static constexpr int bars = kStages * kStageBytes;            // full[kStages], empty[kStages]
   static constexpr int ids = bars + 2 * kStages * 8;            // block ids of the split
   static constexpr int ml = ids + (kMaxSplitTokens / kBlockSize) * 4;  // m, l per warp and row
-  static constexpr int flag = ml + 2 * kConsumerWarps * kRowSlots * 4;
+  static constexpr int flag = ml + 2 * kMmaConsumers * kRowSlots * 4;
   static constexpr int total = flag + 16;
   static constexpr int alloc = total + 1024;  // slack for aligning the base
 };
-static_assert(kConsumerWarps * kRowSlots * kCombineStride * 4 <= kStages * kStageBytes,
+static_assert(kMmaConsumers * kRowSlots * kCombineStride * 4 <= kStages * kStageBytes,
               "cross-warp buffer must fit in the stage ring");
-
-// Byte offset of (token row t, 16-byte chunk c of 16) inside a K or V tile:
-// chunk c lives in box c / 8; within a box, 128-byte rows are swizzled by
-// XOR-ing the chunk index with (row & 7).
-__device__ __forceinline__ uint32_t tile_off(int t, int c) {
-  return uint32_t((c >> 3) * kHalfTile + t * 128 + (((c & 7) ^ (t & 7)) << 4));
-}
+// Every phase of a stage's full barrier must be awaited by the same consumer
+// warp (block j uses stage j % kStages and warp j % kMmaConsumers). Otherwise
+// a fast warp could wait for phase k of a stage whose phase k-1 (another
+// warp's block) has not completed yet, and the parity test would pass early.
+static_assert(kStages % kMmaConsumers == 0, "stages must be a multiple of the consumer warps");
 
 template <int NT>
-__global__ void __launch_bounds__(kMmaThreads, NT == 1 ? 3 : 2)
+__global__ void __launch_bounds__(kMmaThreads, NT == 1 ? 4 : 3)
     attn_mma_kernel(const __grid_constant__ CUtensorMap tmap_k,
                     const __grid_constant__ CUtensorMap tmap_v, const AttnParams p) {
   extern __shared__ uint8_t smem_raw[];
@@ -73,7 +74,7 @@ __global__ void __launch_bounds__(kMmaThreads, NT == 1 ? 3 : 2)
   uint8_t* sbase = smem_raw + (base - raw);
   int32_t* s_ids = reinterpret_cast<int32_t*>(sbase + MmaSmem::ids);
   float* s_m = reinterpret_cast<float*>(sbase + MmaSmem::ml);
-  float* s_l = s_m + kConsumerWarps * kRowSlots;
+  float* s_l = s_m + kMmaConsumers * kRowSlots;
   int* s_flag = reinterpret_cast<int*>(sbase + MmaSmem::flag);
   const uint32_t bar_full = base + MmaSmem::bars;
   const uint32_t bar_empty = bar_full + kStages * 8;
@@ -108,25 +109,12 @@ __global__ void __launch_bounds__(kMmaThreads, NT == 1 ? 3 : 2)
 
   // Consumer state lives at function scope so that it survives until the
   // combine below (the producer warp carries an unused copy).
-  float o[8][NT][4];
-  float m_run[NT][2], l_run[NT][2];
-#pragma unroll
-  for (int mt = 0; mt < 8; ++mt)
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-      for (int e = 0; e < 4; ++e) o[mt][nt][e] = 0.f;
-#pragma unroll
-  for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-    for (int e = 0; e < 2; ++e) {
-      m_run[nt][e] = -INFINITY;
-      l_run[nt][e] = 0.f;
-    }
-  const int g = lane >> 2;  // MMA group id
-  const int c = lane & 3;   // thread in group
+  RowState<NT> st;
+  st.reset();
+  const Lanes ln(lane);
+  const int g = ln.g, c = ln.c;
 
-  if (warp == kConsumerWarps) {
+  if (warp == kMmaConsumers) {
     // ---------------- producer ----------------
     if (lane == 0) {
       prefetch_tensormap(&tmap_k);
@@ -182,13 +170,9 @@ __global__ void __launch_bounds__(kMmaThreads, NT == 1 ? 3 : 2)
         limit[nt][e] = r < w.nrows ? row_limit(p, w.L, w.row0 + r) : -1;
       }
 
-    // ldmatrix lane roles: matrix mi = lane / 8, row rr = lane % 8.
-    const int mi = lane >> 3, rr = lane & 7;
-    const int k_tok = (mi & 1) * 8 + rr, k_chunk = mi >> 1;  // K as A: (tokens, dims)
-    const int v_tok = (mi >> 1) * 8 + rr, v_chunk = mi & 1;  // V^T as A via .trans
     const int new0 = w.L - p.num_queries;  // first position of a new (verify) token
 
-    for (int j = warp; j < nblk; j += kConsumerWarps) {
+    for (int j = warp; j < nblk; j += kMmaConsumers) {
       const int s = j % kStages;
       if (!mbar_wait(bar_full + 8 * s, (j / kStages) & 1)) {
         raise_flag(p.status, PA_FLAG_TIMEOUT);
@@ -242,90 +226,7 @@ __global__ void __launch_bounds__(kMmaThreads, NT == 1 ? 3 : 2)
       }
       if (patched) __syncwarp();
 
-      // S^T (16 tokens x 8*NT rows) = K (16 x 128) . Q^T (128 x 8*NT)
-      float sc[NT][4];
-#pragma unroll
-      for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) sc[nt][e] = 0.f;
-#pragma unroll
-      for (int kk = 0; kk < 8; ++kk) {
-        uint32_t a[4];
-        ldsm_x4(kt + tile_off(k_tok, 2 * kk + k_chunk), a[0], a[1], a[2], a[3]);
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt) mma_bf16_16816(sc[nt], a, qb[kk][nt][0], qb[kk][nt][1]);
-      }
-
-      // Scale to base-2 units and mask. sc[nt][0/1]: token g, rows 2c/2c+1;
-      // sc[nt][2/3]: token g+8, same rows.
-      float bmax[NT][2];
-#pragma unroll
-      for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          const int lim = limit[nt][e];
-          const float s0 = (tok0 + g <= lim) ? sc[nt][e] * p.scale_log2 : -INFINITY;
-          const float s1 = (tok0 + g + 8 <= lim) ? sc[nt][e + 2] * p.scale_log2 : -INFINITY;
-          sc[nt][e] = s0;
-          sc[nt][e + 2] = s1;
-          bmax[nt][e] = fmaxf(s0, s1);
-        }
-#pragma unroll
-      for (int off = 4; off < 32; off <<= 1)
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-          for (int e = 0; e < 2; ++e)
-            bmax[nt][e] = fmaxf(bmax[nt][e], __shfl_xor_sync(0xffffffffu, bmax[nt][e], off));
-
-      // Online softmax update. P enters the MMA as a sum of two bf16 parts,
-      // p = hi + lo (hi = bf16(p), lo = bf16(p - hi)), so the weights carry
-      // about 16 mantissa bits: a single bf16 rounding of p (2^-9 relative)
-      // can cost more than the output tolerance when a short context's
-      // weighted V rows cancel.
-      uint32_t pb[NT][2], pl[NT][2];
-#pragma unroll
-      for (int nt = 0; nt < NT; ++nt) {
-        float alpha[2], pr[4];
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          const float m_new = fmaxf(m_run[nt][e], bmax[nt][e]);
-          const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
-          alpha[e] = fast_exp2(m_run[nt][e] - m_use);
-          m_run[nt][e] = m_new;
-          pr[e] = fast_exp2(sc[nt][e] - m_use);
-          pr[e + 2] = fast_exp2(sc[nt][e + 2] - m_use);
-        }
-        const uint32_t x0 = pack_bf16x2(pr[0], pr[1]);  // token g,   rows 2c, 2c+1
-        const uint32_t x1 = pack_bf16x2(pr[2], pr[3]);  // token g+8, rows 2c, 2c+1
-        const uint32_t y0 = pack_bf16x2(pr[0] - bf16_lo(x0), pr[1] - bf16_hi(x0));
-        const uint32_t y1 = pack_bf16x2(pr[2] - bf16_lo(x1), pr[3] - bf16_hi(x1));
-        l_run[nt][0] = alpha[0] * l_run[nt][0] + (pr[0] + pr[2]);
-        l_run[nt][1] = alpha[1] * l_run[nt][1] + (pr[1] + pr[3]);
-        pb[nt][0] = movmatrix_trans(x0);  // P^T (hi): tokens 2c, 2c+1 of row g
-        pb[nt][1] = movmatrix_trans(x1);  // P^T (hi): tokens 8+2c, 9+2c of row g
-        pl[nt][0] = movmatrix_trans(y0);  // P^T (lo)
-        pl[nt][1] = movmatrix_trans(y1);
-#pragma unroll
-        for (int mt = 0; mt < 8; ++mt) {
-          o[mt][nt][0] *= alpha[0];
-          o[mt][nt][1] *= alpha[1];
-          o[mt][nt][2] *= alpha[0];
-          o[mt][nt][3] *= alpha[1];
-        }
-      }
-
-      // O^T (128 dims x 8*NT rows) += V^T (128 x 16 tokens) . P^T (16 x 8*NT)
-#pragma unroll
-      for (int mt = 0; mt < 8; ++mt) {
-        uint32_t a[4];
-        ldsm_x4_trans(vt + tile_off(v_tok, 2 * mt + v_chunk), a[0], a[1], a[2], a[3]);
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-          mma_bf16_16816(o[mt][nt], a, pb[nt][0], pb[nt][1]);
-          mma_bf16_16816(o[mt][nt], a, pl[nt][0], pl[nt][1]);
-        }
-      }
+      attend_block<NT>(kt, vt, qb, limit, tok0, p.scale_log2, ln, st);
 
       // Hand the stage back to the producer. Generic-proxy writes made above
       // must be ordered before the next TMA write into this stage.
@@ -334,13 +235,7 @@ __global__ void __launch_bounds__(kMmaThreads, NT == 1 ? 3 : 2)
       if (lane == 0) mbar_arrive(bar_empty + 8 * s);
     }
 
-    // Row sums were kept per thread (over its tokens); reduce across lanes.
-#pragma unroll
-    for (int off = 4; off < 32; off <<= 1)
-#pragma unroll
-      for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-        for (int e = 0; e < 2; ++e) l_run[nt][e] += __shfl_xor_sync(0xffffffffu, l_run[nt][e], off);
+    st.reduce_l();  // row sums were kept per lane (over its tokens)
   }
   __syncthreads();
 
@@ -358,30 +253,30 @@ __global__ void __launch_bounds__(kMmaThreads, NT == 1 ? 3 : 2)
 
   // Every stage has been consumed; the ring now holds the cross-warp combine.
   float* cbuf = reinterpret_cast<float*>(sbase + MmaSmem::stages);
-  if (warp < kConsumerWarps) {
+  if (warp < kMmaConsumers) {
     float* mine = cbuf + warp * kRowSlots * kCombineStride;
 #pragma unroll
     for (int mt = 0; mt < 8; ++mt)
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) {
         const int r = nt * 8 + 2 * c, d = mt * 16 + g;
-        mine[r * kCombineStride + d] = o[mt][nt][0];
-        mine[(r + 1) * kCombineStride + d] = o[mt][nt][1];
-        mine[r * kCombineStride + d + 8] = o[mt][nt][2];
-        mine[(r + 1) * kCombineStride + d + 8] = o[mt][nt][3];
+        mine[r * kCombineStride + d] = st.o[mt][nt][0];
+        mine[(r + 1) * kCombineStride + d] = st.o[mt][nt][1];
+        mine[r * kCombineStride + d + 8] = st.o[mt][nt][2];
+        mine[(r + 1) * kCombineStride + d + 8] = st.o[mt][nt][3];
       }
     if (g == 0) {
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
-          s_m[warp * kRowSlots + nt * 8 + 2 * c + e] = m_run[nt][e];
-          s_l[warp * kRowSlots + nt * 8 + 2 * c + e] = l_run[nt][e];
+          s_m[warp * kRowSlots + nt * 8 + 2 * c + e] = st.m[nt][e];
+          s_l[warp * kRowSlots + nt * 8 + 2 * c + e] = st.l[nt][e];
         }
     }
   }
   __syncthreads();
-  split_epilogue<uint16_t>(p, w, cbuf, s_m, s_l, kConsumerWarps, s_flag);
+  split_epilogue<uint16_t>(p, w, cbuf, s_m, s_l, kMmaConsumers, s_flag);
 }
 
 size_t mma_smem_bytes() { return MmaSmem::alloc; }

@@ -14,6 +14,7 @@ namespace pa {
 cudaError_t launch_attn_mma(const CUtensorMap& tk, const CUtensorMap& tv, const AttnParams& p,
                             dim3 grid, cudaStream_t stream);
 cudaError_t launch_attn_simt(const AttnParams& p, bool bf16, dim3 grid, cudaStream_t stream);
+cudaError_t launch_attn_ldg(const AttnParams& p, int prefetch, int warps, cudaStream_t stream);
 }  // namespace pa
 
 namespace {
@@ -186,11 +187,16 @@ pa_status attend(const pa_cache* cache, const void* q, void* out, const void* k_
   if (!std::isfinite(scale)) return PA_ERR_INVALID_ARG;
   const int32_t split = split_of(opts);
   if (split % kBlockSize || split > kMaxSplitTokens) return PA_ERR_UNSUPPORTED;
-  const int32_t kernel = opts ? opts->kernel : PA_KERNEL_AUTO;
-  if (kernel < PA_KERNEL_AUTO || kernel > PA_KERNEL_SIMT) return PA_ERR_UNSUPPORTED;
+  int32_t kernel = opts ? opts->kernel : PA_KERNEL_AUTO;
+  if (kernel < PA_KERNEL_AUTO || kernel > PA_KERNEL_MMA_LDG) return PA_ERR_UNSUPPORTED;
   const bool bf16 = cache->dtype == PA_DTYPE_BF16;
-  const bool use_mma = (kernel == PA_KERNEL_MMA) || (kernel == PA_KERNEL_AUTO && bf16);
+  if (kernel == PA_KERNEL_AUTO) kernel = bf16 ? PA_KERNEL_MMA : PA_KERNEL_SIMT;
+  const bool use_mma = kernel == PA_KERNEL_MMA || kernel == PA_KERNEL_MMA_LDG;
   if (use_mma && !bf16) return PA_ERR_UNSUPPORTED;
+  const int32_t prefetch = (opts && opts->prefetch > 0) ? opts->prefetch : PA_DEFAULT_PREFETCH;
+  if (prefetch > 2) return PA_ERR_UNSUPPORTED;
+  const int32_t warps = (opts && opts->warps > 0) ? opts->warps : PA_DEFAULT_WARPS;
+  if (warps != 1 && warps != 2 && warps != 4) return PA_ERR_UNSUPPORTED;
   if (batch == 0) return PA_OK;
   if (!q || !out || !tables || !lens || !aligned16(q) || !aligned16(out)) return PA_ERR_INVALID_ARG;
   if (mbps <= 0 || int64_t(max_ctx) > int64_t(mbps) * kBlockSize) return PA_ERR_INVALID_ARG;
@@ -236,12 +242,15 @@ pa_status attend(const pa_cache* cache, const void* q, void* out, const void* k_
   p.scale_log2 = scale * 1.4426950408889634f;
 
   const int64_t gz = int64_t(batch) * p.row_groups;
-  if (gz > 65535) return PA_ERR_UNSUPPORTED;
+  if (kernel != PA_KERNEL_MMA_LDG && gz > 65535) return PA_ERR_UNSUPPORTED;
+  if (int64_t(batch) * cache->kv_heads * p.row_groups * L.max_splits > INT32_MAX) return PA_ERR_UNSUPPORTED;
   const dim3 grid(unsigned(L.max_splits), unsigned(cache->kv_heads), unsigned(gz));
   cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
 
   cudaError_t e;
-  if (use_mma) {
+  if (kernel == PA_KERNEL_MMA_LDG) {
+    e = launch_attn_ldg(p, prefetch, warps, stream);
+  } else if (kernel == PA_KERNEL_MMA) {
     CUtensorMap tk, tv;
     if (!make_pool_map(&tk, cache->k, cache->kv_heads, cache->num_blocks) ||
         !make_pool_map(&tv, cache->v, cache->kv_heads, cache->num_blocks))

@@ -38,7 +38,7 @@ def test_every_declared_symbol_is_exported(lib):
 def test_header_constants_match_binding():
     text = HEADER.read_text()
     for name in ("PA_FLAG_BAD_BLOCK", "PA_FLAG_BAD_LENGTH", "PA_FLAG_BAD_SLOT", "PA_FLAG_TIMEOUT",
-                 "PA_DEFAULT_SPLIT_TOKENS", "PA_VALIDATE_WORDS"):
+                 "PA_DEFAULT_SPLIT_TOKENS", "PA_VALIDATE_WORDS", "PA_DEFAULT_PREFETCH"):
         m = re.search(rf"#define {name} (0x[0-9a-f]+|\d+)", text)
         assert m and int(m.group(1), 0) == getattr(_lib, name), name
 
@@ -83,6 +83,8 @@ def test_bad_call_arguments_rejected(lib):
     assert _decode(lib, c, opts=_lib.PaOptions(0, 9)) == _lib.PA_ERR_UNSUPPORTED
     f32 = _cache(dtype=_lib.PA_DTYPE_F32)
     assert _decode(lib, f32, opts=_lib.PaOptions(0, _lib.PA_KERNEL_MMA)) == _lib.PA_ERR_UNSUPPORTED
+    assert _decode(lib, f32, opts=_lib.PaOptions(0, _lib.PA_KERNEL_MMA_LDG)) == _lib.PA_ERR_UNSUPPORTED
+    assert _decode(lib, c, opts=_lib.PaOptions(0, 0, 3)) == _lib.PA_ERR_UNSUPPORTED   # prefetch > 2
     assert _decode(lib, c, batch=0) == _lib.PA_OK                      # nothing to do, nothing launched
 
 

@@ -9,7 +9,7 @@ from paged_kv_decode_pa_gb300 import inputs
 pytestmark = pytest.mark.gpu
 
 
-@pytest.mark.parametrize("kernel", ["auto", "simt"])
+@pytest.mark.parametrize("kernel", ["auto", "mma_ldg", "simt"])
 def test_verify_c5_matches_oracle(kernel):
     w = workload("c5")
     ref, okc, ovc = oracle_verify_of(w)
@@ -29,9 +29,10 @@ def test_verify_shapes(nq, hq, hkv, split):
     if nq == 1:
         w.q = w.q[:, None]
     ref, okc, ovc = oracle_verify_of(w)
-    out, gk, gv = gpu_verify(w, split_tokens=split)
-    assert gk.tobytes() == okc.tobytes() and gv.tobytes() == ovc.tobytes()
-    assert_close(to_f64(out), ref, "bf16", f"verify nq={nq} {hq}/{hkv} split {split}")
+    for kernel, warps in (("auto", 0), ("mma_ldg", 1), ("mma_ldg", 0)):
+        out, gk, gv = gpu_verify(w, split_tokens=split, kernel=kernel, warps=warps)
+        assert gk.tobytes() == okc.tobytes() and gv.tobytes() == ovc.tobytes()
+        assert_close(to_f64(out), ref, "bf16", f"verify nq={nq} {hq}/{hkv} {kernel} split {split}")
 
 
 def test_verify_fp32():

@@ -57,6 +57,8 @@ def parse_args():
     ap.add_argument("--prefetch", type=int, default=0, help="blocks in flight per warp (mma_ldg kernel)")
     ap.add_argument("--warps", type=int, default=0, help="warps per split (mma_ldg kernel)")
     ap.add_argument("--split-tokens", type=int, default=0)
+    ap.add_argument("--graph", action="store_true",
+                    help="time each step as a replay of a captured CUDA graph of the step")
     ap.add_argument("--unfused", action="store_true",
                     help="time a decode step as two calls, pa_cache_write then pa_decode")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="CPU baseline sample budget")
@@ -249,6 +251,23 @@ class DecodeStep:
             self.write()
         self.attend()
 
+    def capture(self):
+        """Record one step in a CUDA graph, as an engine does per batch bucket
+        ("From 183 ms to 19 ms per decode step", section "4. CUDA graphs per
+        batch bucket"); every buffer the graph reads is owned by this object."""
+        import torch
+
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            self.run()  # warm the library's per-device set-up outside the capture
+        torch.cuda.current_stream().wait_stream(side)
+        torch.cuda.synchronize()
+        self.graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.graph):
+            self.run()
+        torch.cuda.synchronize()
+
 
 def make_l2_flush(device):
     """Return a function that leaves L2 holding nothing the timed step reads.
@@ -280,14 +299,34 @@ def gpu_hold(us: float = 150.0):
         sleep(int(us * 2000))  # cycles at about 2 GHz
 
 
-def time_steps(step: DecodeStep, steps: int, warmup: int, flush):
-    """Per-step CUDA-event times (ms) of the whole step and of its attention call."""
+def time_steps(step: DecodeStep, steps: int, warmup: int, flush, graph: bool = False):
+    """Per-step CUDA-event times (ms) of the whole step and of its attention call.
+
+    With graph=True each step is one replay of the captured step graph (both
+    returned lists are then the replay time).
+    """
     import torch
 
     for _ in range(warmup):
         flush()
         step.run()
     torch.cuda.synchronize()
+    if graph:
+        step.capture()
+        for _ in range(warmup):
+            flush()
+            step.graph.replay()
+        torch.cuda.synchronize()
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(steps)]
+        for k in range(steps):
+            flush()
+            gpu_hold()
+            ev[k][0].record()
+            step.graph.replay()
+            ev[k][1].record()
+        torch.cuda.synchronize()
+        t = [e[0].elapsed_time(e[1]) for e in ev]
+        return t, t
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
     for k in range(steps):
         flush()
@@ -348,10 +387,10 @@ def step_bytes(w, fused=True):
     return att, write
 
 
-def measure_extra(name, device, steps, flush, split, kernel, prefetch=0, warps=0, fused=True):
+def measure_extra(name, device, steps, flush, split, kernel, prefetch=0, warps=0, fused=True, graph=False):
     w = inputs.make(name)
     st = DecodeStep(w, device, split, kernel, prefetch, warps, fused)
-    total, attend = time_steps(st, steps, 3, flush)
+    total, attend = time_steps(st, steps, 3, flush, graph)
     att, _ = step_bytes(w, fused)
     us = statistics.mean(attend) * 1e3
     peak, _ = hbm_peak()
@@ -390,7 +429,7 @@ def run_native(args):
     torch.cuda.synchronize()
     with ClockSampler(local) as clocks:
         t0 = time.perf_counter()
-        total, attend = time_steps(step, args.steps, args.warmup, flush)
+        total, attend = time_steps(step, args.steps, args.warmup, flush, args.graph)
         wall = time.perf_counter() - t0
     torch.cuda.synchronize()
     barrier(world)
@@ -414,7 +453,7 @@ def run_native(args):
         for name in ("c2", "c3", "c5"):
             if name != args.workload:
                 extra[name] = measure_extra(name, device, 20, flush, args.split_tokens, args.kernel,
-                                            args.prefetch, args.warps, not args.unfused)
+                                            args.prefetch, args.warps, not args.unfused, args.graph)
 
     cpu = cpu_baseline(w, args.cpu_seconds) if rank == 0 else None
 
@@ -441,6 +480,7 @@ def run_native(args):
                 "context_tokens": int(w.context_lens.sum()),
                 "split_tokens": args.split_tokens or _lib.PA_DEFAULT_SPLIT_TOKENS,
                 "kernel": args.kernel,
+                "launch": "CUDA graph replay of the step" if args.graph else "direct launches",
                 **({"prefetch": args.prefetch or 1, "warps_per_split": args.warps or 4}
                    if args.kernel == "mma_ldg" else {}),
                 "step": ("pa_cache_write (one new token per sequence) + pa_decode" if not step.fused

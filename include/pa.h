@@ -126,7 +126,7 @@ typedef struct pa_options {
 #define PA_DEFAULT_PREFETCH 1
 #define PA_DEFAULT_WARPS 4
 
-#define PA_DEFAULT_SPLIT_TOKENS 1024
+#define PA_DEFAULT_SPLIT_TOKENS 1536
 
 /*
  * pa_cache_write: cache[h, s / 16, s % 16, :] = new[i, h, :] for every token

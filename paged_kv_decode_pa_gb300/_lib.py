@@ -32,7 +32,7 @@ PA_FLAG_BAD_LENGTH = 0x2
 PA_FLAG_BAD_SLOT = 0x4
 PA_FLAG_TIMEOUT = 0x8
 
-PA_DEFAULT_SPLIT_TOKENS = 1024
+PA_DEFAULT_SPLIT_TOKENS = 1536
 PA_VALIDATE_WORDS = 4
 PA_NOALLOC_SCRATCH_BYTES = 16 << 20
 

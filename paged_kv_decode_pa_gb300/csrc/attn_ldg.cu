@@ -38,20 +38,14 @@
 
 namespace pa {
 
+cudaError_t launch_merge(const AttnParams& p, cudaStream_t stream);
+
 __device__ __forceinline__ uint4 ld_stream(const void* ptr) {
   uint4 v;
   asm volatile("ld.global.nc.L1::no_allocate.L2::256B.v4.u32 {%0, %1, %2, %3}, [%4];"
                : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
                : "l"(ptr));
   return v;
-}
-
-__device__ __forceinline__ void pdl_launch_dependents() {
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-}
-
-__device__ __forceinline__ void pdl_wait_primary() {
-  asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
 template <int NT, int W>
@@ -304,75 +298,6 @@ __global__ void __launch_bounds__(32 * W, ((NT == 1 && PF == 1) ? 12 : 8) / W)
   pdl_launch_dependents();
 }
 
-// Log-sum-exp merge of the split partials of every (sequence, KV head, row
-// group) with more than one split. One CTA per (unit, row); warp w takes
-// splits w, w+8, ...; a lane holds 4 dims. Launched as a programmatic
-// dependent of the attention kernel: it waits for that grid before reading.
-constexpr int kMergeWarps = 8;
-
-__global__ void __launch_bounds__(kMergeWarps * 32) merge_kernel(const AttnParams p) {
-  pdl_wait_primary();
-  __shared__ float s_max[kMergeWarps], s_den[kMergeWarps];
-  __shared__ __align__(16) float s_acc[kMergeWarps][kHeadDim];
-  const int unit = blockIdx.x, r = blockIdx.y;
-  const int rg = unit % p.row_groups;
-  const int bh = unit / p.row_groups;
-  const int h = bh % p.kv_heads, b = bh / p.kv_heads;
-  const int row0 = rg * p.rows_per_cta;
-  const int nrows = min(p.rows_per_cta, p.rows - row0);
-  if (r >= nrows) return;
-  int L = __ldg(p.context_lens + b);
-  const int cap = min(p.max_context_len, p.mbps * kBlockSize);
-  L = L < 0 ? 0 : min(L, cap);
-  const int nsplit = (L + p.split_tokens - 1) / p.split_tokens;
-  if (nsplit <= 1) return;  // written directly by the attention kernel
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const size_t base = size_t(unit) * p.max_splits;
-
-  float mx = -INFINITY;
-  for (int s = warp; s < nsplit; s += kMergeWarps)
-    mx = fmaxf(mx, __ldcg(p.part_lse + (base + s) * kRowSlots + r));
-  if (lane == 0) s_max[warp] = mx;
-  __syncthreads();
-  float M = -INFINITY;
-#pragma unroll
-  for (int w = 0; w < kMergeWarps; ++w) M = fmaxf(M, s_max[w]);
-
-  float den = 0.f, acc[4] = {0.f, 0.f, 0.f, 0.f};
-  if (M != -INFINITY) {
-#pragma unroll 4
-    for (int s = warp; s < nsplit; s += kMergeWarps) {
-      const float lse = __ldcg(p.part_lse + (base + s) * kRowSlots + r);
-      const float4 v =
-          __ldcg(reinterpret_cast<const float4*>(p.part_o + ((base + s) * kRowSlots + r) * kHeadDim) + lane);
-      const float wgt = fast_exp2(lse - M);
-      den += wgt;
-      acc[0] += wgt * v.x;
-      acc[1] += wgt * v.y;
-      acc[2] += wgt * v.z;
-      acc[3] += wgt * v.w;
-    }
-  }
-  if (lane == 0) s_den[warp] = den;
-  *reinterpret_cast<float4*>(&s_acc[warp][lane * 4]) = make_float4(acc[0], acc[1], acc[2], acc[3]);
-  __syncthreads();
-  if (warp == 0) {
-    float d = 0.f, v[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-    for (int w = 0; w < kMergeWarps; ++w) {
-      d += s_den[w];
-#pragma unroll
-      for (int e = 0; e < 4; ++e) v[e] += s_acc[w][lane * 4 + e];
-    }
-    const float iv = d > 0.f ? 1.f / d : 0.f;
-    uint16_t* dst = static_cast<uint16_t*>(p.out) + row_offset(p, b, h, row0 + r) + lane * 4;
-    uint2 u;
-    u.x = pack_bf16x2(v[0] * iv, v[1] * iv);
-    u.y = pack_bf16x2(v[2] * iv, v[3] * iv);
-    *reinterpret_cast<uint2*>(dst) = u;
-  }
-}
-
 template <int NT, int PF>
 static void launch_w(const AttnParams& p, int warps, unsigned grid, cudaStream_t stream) {
   if (warps >= 4)
@@ -398,20 +323,9 @@ cudaError_t launch_attn_ldg(const AttnParams& p, int prefetch, int warps, cudaSt
     launch_w<1, 2>(p, warps, grid, stream);
   else
     launch_w<1, 1>(p, warps, grid, stream);
-  cudaError_t e = cudaGetLastError();
+  const cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess || p.max_splits <= 1) return e;
-
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(unsigned(p.batch * p.kv_heads * p.row_groups), unsigned(p.rows_per_cta), 1);
-  cfg.blockDim = dim3(kMergeWarps * 32, 1, 1);
-  cfg.dynamicSmemBytes = 0;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, merge_kernel, p);
+  return launch_merge(p, stream);
 }
 
 }  // namespace pa

@@ -79,24 +79,26 @@ __global__ void __launch_bounds__(kMmaThreads, NT == 1 ? 4 : 3)
   const uint32_t bar_full = base + MmaSmem::bars;
   const uint32_t bar_empty = bar_full + kStages * 8;
 
-  const CtaWork w = cta_work(p);
+  // The sequence's length and the split's block-table entries are loaded
+  // together: the entries a split may use do not depend on the length, so the
+  // two memory latencies overlap instead of adding up.
+  int L_raw;
+  {
+    const int b = blockIdx.z / p.row_groups;
+    const int per = p.split_tokens / kBlockSize;
+    const int j0 = blockIdx.x * per;
+    const int jn = min(per, p.mbps - j0);
+    L_raw = __ldg(p.context_lens + b);
+    for (int j = threadIdx.x; j < jn; j += blockDim.x)
+      s_ids[j] = __ldg(p.block_tables + int64_t(b) * p.mbps + j0 + j);
+  }
+  const CtaWork w = cta_work(p, L_raw);
   if (w.split >= w.nsplit) {
     if (w.L == 0 && w.split == 0) write_zero_rows<uint16_t>(p, w);
     return;
   }
   const int nblk = (w.t1 - w.t0 + kBlockSize - 1) / kBlockSize;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-
-  // Block ids of this split; a bad id is replaced by a coordinate outside the
-  // tensor, which TMA fills with zeros.
-  for (int j = threadIdx.x; j < nblk; j += blockDim.x) {
-    int id = __ldg(p.block_tables + int64_t(w.b) * p.mbps + w.t0 / kBlockSize + j);
-    if (id < 0 || id >= p.num_blocks) {
-      raise_flag(p.status, PA_FLAG_BAD_BLOCK);
-      id = -1;
-    }
-    s_ids[j] = id;
-  }
   if (threadIdx.x == 0) {
     s_flag[0] = s_flag[1] = s_flag[2] = s_flag[3] = 0;
     for (int s = 0; s < kStages; ++s) {
@@ -130,7 +132,11 @@ __global__ void __launch_bounds__(kMmaThreads, NT == 1 ? 4 : 3)
         }
         const uint32_t st = base + MmaSmem::stages + s * kStageBytes;
         const uint32_t fb = bar_full + 8 * s;
-        const int id = s_ids[j];
+        int id = s_ids[j];
+        if (id < 0 || id >= p.num_blocks) {  // outside the pool: TMA reads zeros instead
+          raise_flag(p.status, PA_FLAG_BAD_BLOCK);
+          id = -1;
+        }
         const int y = id >= 0 ? id * kBlockSize : -kBlockSize;
         mbar_arrive_expect_tx(fb, kStageBytes);
         tma_load_3d(st, &tmap_k, 0, y, w.h, fb, policy);
@@ -238,6 +244,7 @@ __global__ void __launch_bounds__(kMmaThreads, NT == 1 ? 4 : 3)
     st.reduce_l();  // row sums were kept per lane (over its tokens)
   }
   __syncthreads();
+  pdl_launch_dependents();  // the merge kernel (if any) may start launching
 
   if (s_flag[2]) {
     // A wait gave up: let every load already issued land (bounded) before the

@@ -15,6 +15,7 @@ cudaError_t launch_attn_mma(const CUtensorMap& tk, const CUtensorMap& tv, const 
                             dim3 grid, cudaStream_t stream);
 cudaError_t launch_attn_simt(const AttnParams& p, bool bf16, dim3 grid, cudaStream_t stream);
 cudaError_t launch_attn_ldg(const AttnParams& p, int prefetch, int warps, cudaStream_t stream);
+cudaError_t launch_merge(const AttnParams& p, cudaStream_t stream);
 }  // namespace pa
 
 namespace {
@@ -53,6 +54,7 @@ int32_t split_of(const pa_options* o) {
 // kernel, an upper bound for the 16-row tensor-core kernel.
 struct WsLayout {
   size_t counters, lse, o, total;
+  int64_t units;
   int32_t max_splits;
 };
 
@@ -68,6 +70,7 @@ bool ws_layout(int32_t batch, int32_t nq, int32_t q_heads, int32_t kv_heads, int
   const int64_t units = int64_t(batch) * kv_heads * groups;
   WsLayout L;
   L.max_splits = static_cast<int32_t>(splits);
+  L.units = units;
   L.counters = 256;
   L.lse = L.counters + round256(size_t(units) * 4);
   L.o = L.lse + round256(size_t(units * splits * kRowSlots) * 4);
@@ -239,6 +242,9 @@ pa_status attend(const pa_cache* cache, const void* q, void* out, const void* k_
   p.split_tokens = split;
   p.max_splits = L.max_splits;
   p.fused_write = fused ? 1 : 0;
+  // The CUDA-core kernel merges in its last split; the tensor-core kernels
+  // leave the merge to merge_kernel.
+  p.merge_in_kernel = kernel == PA_KERNEL_SIMT ? 1 : 0;
   p.scale_log2 = scale * 1.4426950408889634f;
 
   const int64_t gz = int64_t(batch) * p.row_groups;
@@ -256,6 +262,7 @@ pa_status attend(const pa_cache* cache, const void* q, void* out, const void* k_
         !make_pool_map(&tv, cache->v, cache->kv_heads, cache->num_blocks))
       return cuda_fail(cudaErrorInvalidValue);
     e = launch_attn_mma(tk, tv, p, grid, stream);
+    if (e == cudaSuccess && p.max_splits > 1) e = launch_merge(p, stream);
   } else {
     e = launch_attn_simt(p, bf16, grid, stream);
   }

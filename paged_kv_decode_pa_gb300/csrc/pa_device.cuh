@@ -46,6 +46,7 @@ struct AttnParams {
   int32_t row_groups;  // ceil(rows / rows_per_cta)
   int32_t max_context_len, split_tokens, max_splits;
   int32_t fused_write;  // 1: new rows come from k_new/v_new and are written to the cache
+  int32_t merge_in_kernel;  // 1: the last split to finish merges; 0: merge_kernel does
   float scale_log2;     // scale * log2(e): scores are kept in base-2 units
 };
 
@@ -174,6 +175,16 @@ __device__ __forceinline__ float fast_exp2(float x) {
   return y;
 }
 
+// Programmatic dependent launch: let the next kernel on the stream start
+// launching, and (in that kernel) wait until this one's writes are visible.
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+__device__ __forceinline__ void pdl_wait_primary() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 __device__ __forceinline__ void raise_flag(uint32_t* status, uint32_t bits) {
   if (status) atomicOr(status, bits);
 }
@@ -191,13 +202,15 @@ struct CtaWork {
   int unit;       // (b * kv_heads + h) * row_groups + rg
 };
 
-__device__ __forceinline__ CtaWork cta_work(const AttnParams& p) {
+// The work of CTA (blockIdx.x = split, .y = KV head, .z = sequence x row
+// group); L_raw is context_lens[b] if the caller has loaded it already.
+__device__ __forceinline__ CtaWork cta_work(const AttnParams& p, int L_raw = -2147483647 - 1) {
   CtaWork w;
   w.split = blockIdx.x;
   w.h = blockIdx.y;
   w.b = blockIdx.z / p.row_groups;
   w.rg = blockIdx.z - w.b * p.row_groups;
-  int L = __ldg(p.context_lens + w.b);
+  int L = L_raw == -2147483647 - 1 ? __ldg(p.context_lens + w.b) : L_raw;
   const int cap = min(p.max_context_len, p.mbps * kBlockSize);
   if (L < 0 || L > cap) {
     if (w.split == 0 && w.h == 0 && w.rg == 0) raise_flag(p.status, PA_FLAG_BAD_LENGTH);
@@ -300,7 +313,7 @@ __device__ void split_epilogue(const AttnParams& p, const CtaWork& w, const floa
       if (c == 0) p.part_lse[slot * kRowSlots + r] = l > 0.f ? M + __log2f(l) : -INFINITY;
     }
   }
-  if (single) return;
+  if (single || !p.merge_in_kernel) return;
 
   // Publish this split, then count arrivals; the last arrival merges.
   __threadfence();

@@ -91,7 +91,7 @@ def test_zero_length_gives_zeros():
 
 
 def test_max_sizes_single_sequence_long():
-    """Largest context the default plan handles in one row: 64 splits of 512 plus a tail."""
+    """One long sequence: many default-size splits plus a ragged tail, merged."""
     L = 32768 + 17
     w = inputs.custom(batch=1, q_heads=12, kv_heads=2, context_lens=(L,), num_blocks=(L + 15) // 16 + 1,
                       dtype="bf16", seed=9)

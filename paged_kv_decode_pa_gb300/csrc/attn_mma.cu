@@ -79,6 +79,12 @@ __global__ void __launch_bounds__(kMmaThreads, NT == 1 ? 4 : 3)
   const uint32_t bar_full = base + MmaSmem::bars;
   const uint32_t bar_empty = bar_full + kStages * 8;
 
+  // The descriptor fetch overlaps the loads below instead of delaying the
+  // first TMA issue.
+  if (threadIdx.x == kMmaConsumers * 32) {
+    prefetch_tensormap(&tmap_k);
+    prefetch_tensormap(&tmap_v);
+  }
   // The sequence's length and the split's block-table entries are loaded
   // together: the entries a split may use do not depend on the length, so the
   // two memory latencies overlap instead of adding up.
@@ -119,8 +125,6 @@ __global__ void __launch_bounds__(kMmaThreads, NT == 1 ? 4 : 3)
   if (warp == kMmaConsumers) {
     // ---------------- producer ----------------
     if (lane == 0) {
-      prefetch_tensormap(&tmap_k);
-      prefetch_tensormap(&tmap_v);
       const uint64_t policy = policy_evict_first();
       int issued = 0;
       for (int j = 0; j < nblk; ++j) {

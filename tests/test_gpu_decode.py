@@ -90,13 +90,15 @@ def test_zero_length_gives_zeros():
     assert_close(to_f64(out), ref, "bf16", "zero length")
 
 
-def test_max_sizes_single_sequence_long():
-    """One long sequence: many default-size splits plus a ragged tail, merged."""
+@pytest.mark.parametrize("split", [0, 64])
+def test_max_sizes_single_sequence_long(split):
+    """One long sequence: many splits plus a ragged tail, merged (split 64 gives
+    513 splits, more than one 256-split chunk of the merge)."""
     L = 32768 + 17
     w = inputs.custom(batch=1, q_heads=12, kv_heads=2, context_lens=(L,), num_blocks=(L + 15) // 16 + 1,
                       dtype="bf16", seed=9)
     kc, vc = w.k_cache.copy(), w.v_cache.copy()
     oracle.cache_write(kc, vc, w.k_new, w.v_new, w.slot_mapping)
     ref = oracle.decode(kc, vc, w.q, w.block_tables, w.context_lens, w.scale)
-    out, _, _ = gpu_decode(w)
-    assert_close(to_f64(out), ref, "bf16", "long single")
+    out, _, _ = gpu_decode(w, split_tokens=split)
+    assert_close(to_f64(out), ref, "bf16", f"long single split {split}")

@@ -1,8 +1,9 @@
 """Benchmark of the paged-KV decode hot path on GB300.
 
-One step = the whole hot path over one batch: pa_cache_write of the step's new
-tokens, then pa_decode over every sequence's paged context (inputs resident in
-HBM). The headline workload is the 32k-context decode (8 sequences x 32768
+One step = the whole hot path over one batch: the append of each sequence's
+new token and the decode over its paged context, as one fused call (pa_verify
+with one query per sequence; --unfused times pa_cache_write then pa_decode),
+with the inputs resident in HBM. The headline workload is the 32k-context decode (8 sequences x 32768
 tokens, 12 query / 2 KV heads, head_dim 128, bf16, 16384-block pool). The
 64-sequence decode, the Qwen2-1.5B-shaped decode and the fused speculative
 verify are measured too and reported under "per_config".
@@ -88,6 +89,18 @@ def barrier(world):
         import torch.distributed as dist
 
         dist.barrier()
+
+
+def rank_workload(name: str, rank: int):
+    """This rank's replica of a workload: same shapes, its own seed (weak scaling)."""
+    base = inputs.CONFIGS[name]
+    return inputs.generate(base, seed=base.seed + 1000 * rank)
+
+
+def whole_job_gbs(kv_bytes_per_rank: int, world: int, ms_step_max: float) -> float:
+    """Whole-job KV-read rate: the bytes every rank read in one step, over the
+    slowest rank's step time."""
+    return kv_bytes_per_rank * world / (ms_step_max * 1e-3) / 1e9
 
 
 def max_over_ranks(x: float, world: int, device) -> float:
@@ -230,6 +243,16 @@ class DecodeStep:
         self.ws = pa.new_workspace(s.batch, self.nq, s.q_heads, s.kv_heads, w.max_context_len, device,
                                    split_tokens)
 
+    def rebind(self, q, k_new, v_new, slots, tables, lens):
+        """A copy of this step that reads its per-step inputs from other device
+        tensors (same shapes); caches, output and workspace are shared."""
+        import copy
+
+        st = copy.copy(self)
+        st.q, st.k_new, st.v_new, st.slots, st.tables, st.lens = q, k_new, v_new, slots, tables, lens
+        st.q4 = q if q.dim() == 4 else q.unsqueeze(1)
+        return st
+
     def write(self):
         self.pa.pa_cache_write(self.kc, self.vc, self.k_new, self.v_new, self.slots)
 
@@ -344,24 +367,31 @@ def time_steps(step: DecodeStep, steps: int, warmup: int, flush, graph: bool = F
 
 
 def time_e2e(step: DecodeStep, steps: int, warmup: int, flush):
-    """Same step through the public API from pinned host buffers, copies inside the timed region."""
+    """The same step through the public API from pinned host memory: every step
+    uploads its small inputs (q, new K/V rows, slots, block tables, lengths) with
+    one copy from a pinned staging buffer, calls libpa on the device views, and
+    copies the output back; both copies are inside the timed region."""
     import torch
+
+    from paged_kv_decode_pa_gb300.staging import StepStaging
 
     pa = step.pa
     w = step.w
-    host = {name: pa.to_torch(getattr(w, name), "cpu").pin_memory()
-            for name in ("q", "k_new", "v_new", "slot_mapping", "block_tables", "context_lens")}
-    dev = {"q": step.q, "k_new": step.k_new, "v_new": step.v_new, "slot_mapping": step.slots,
-           "block_tables": step.tables, "context_lens": step.lens}
+    names = ("q", "k_new", "v_new", "slot_mapping", "block_tables", "context_lens")
+    tens = {n: pa.to_torch(getattr(w, n), "cpu") for n in names}
+    stage = StepStaging({n: (tuple(t.shape), t.dtype) for n, t in tens.items()}, step.dev)
+    for n, t in tens.items():
+        stage.host[n].copy_(t)
+    d = stage.dev
+    view = step.rebind(d["q"], d["k_new"], d["v_new"], d["slot_mapping"], d["block_tables"], d["context_lens"])
     out_host = torch.empty(step.out.shape, dtype=step.out.dtype).pin_memory()
-    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    h2d = stage.upload_bytes
     d2h = out_host.numel() * out_host.element_size()
 
     def one():
-        for name, t in host.items():
-            dev[name].copy_(t, non_blocking=True)
-        step.run()
-        out_host.copy_(step.out, non_blocking=True)
+        stage.upload()
+        view.run()
+        out_host.copy_(view.out, non_blocking=True)
 
     for _ in range(warmup):
         flush()
@@ -401,9 +431,15 @@ def measure_extra(name, device, steps, flush, split, kernel, prefetch=0, warps=0
            "kv_bytes": att["kv"], "algorithmic_bytes": att["total"],
            "kv_gbs": round(att["kv"] / (us * 1e-6) / 1e9, 1), "achieved_gbs": round(gbs, 1),
            "frac_of_measured_hbm": round(gbs / peak, 3), "frac_of_8tbs": round(gbs / 8000.0, 3),
+           "us_per_call_median": round(statistics.median(attend) * 1e3, 2),
            "call": ("pa_verify (fused write)" if w.spec.num_queries > 1 else
                     "pa_verify, one query per sequence (fused append + decode)" if fused else "pa_decode"),
            "l2": "flushed (write + read) before each call"}
+    # Warm variant: no flush between calls, so whatever of the working set
+    # fits in L2 (129 MB) is read from there.
+    _, warm = time_steps(st, steps, 3, lambda: None, graph)
+    rec["warm_us_per_call"] = round(statistics.mean(warm) * 1e3, 2)
+    rec["warm_achieved_gbs"] = round(att["total"] / (statistics.mean(warm) * 1e-3) / 1e9, 1)
     del st
     return rec
 
@@ -418,8 +454,7 @@ def run_native(args):
     from paged_kv_decode_pa_gb300 import _lib
 
     _lib.load()  # fails loudly if the library is missing
-    base = inputs.CONFIGS[args.workload]
-    w = inputs.generate(base, seed=base.seed + 1000 * rank)
+    w = rank_workload(args.workload, rank)
     step = DecodeStep(w, device, args.split_tokens, args.kernel, args.prefetch, args.warps,
                       fused=not args.unfused)
     flush = make_l2_flush(device)
@@ -442,8 +477,7 @@ def run_native(args):
     e2e_ms, h2d, d2h = time_e2e(step, max(5, args.steps // 2), 3, flush)
     e2e_step = max_over_ranks(statistics.mean(e2e_ms), world, device)
 
-    kv_total = att["kv"] * world
-    value = kv_total / (ms_step * 1e-3) / 1e9
+    value = whole_job_gbs(att["kv"], world, ms_step)
     peak, peak_kind = hbm_peak()
     achieved = att["total"] / (ms_attend * 1e-3) / 1e9
     traffic = ncu_traffic(args.workload)
@@ -468,6 +502,9 @@ def run_native(args):
             "warmup": args.warmup,
             "ms_per_step": round(ms_step, 5),
             "us_per_call": round(ms_attend * 1e3, 2),
+            "us_per_call_median": round(statistics.median(attend) * 1e3, 2),
+            "us_per_call_p10_p90": [round(float(np.percentile(attend, 10)) * 1e3, 2),
+                                    round(float(np.percentile(attend, 90)) * 1e3, 2)],
             "higher_is_better": True,
             "scaling": "weak",
             "vs_baseline": None,
@@ -506,9 +543,9 @@ def run_native(args):
                 "traffic": traffic,
             },
             "cpu_baseline": cpu,
-            "e2e": {"value": round(kv_total / (e2e_step * 1e-3) / 1e9, 1), "unit": "GB/s",
+            "e2e": {"value": round(whole_job_gbs(att["kv"], world, e2e_step), 1), "unit": "GB/s",
                     "ms_per_step": round(e2e_step, 5), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                    "path": "pinned host -> device copies of the step's inputs, the step's libpa call(s), "
+                    "path": "one pinned host -> device copy of the step's inputs (StepStaging), the step's libpa call(s), "
                             "device -> host copy of the output"},
             "gpu_launches": ((0 if step.fused else 1) + 1
                              + (1 if args.kernel == "mma_ldg" and w.max_context_len > (args.split_tokens or

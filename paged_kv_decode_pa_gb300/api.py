@@ -8,6 +8,7 @@ memory and streams; nothing here computes attention.
 from __future__ import annotations
 
 import ctypes
+import functools
 from typing import Optional
 
 import numpy as np
@@ -21,12 +22,21 @@ _KERNELS = {"auto": L.PA_KERNEL_AUTO, "mma": L.PA_KERNEL_MMA, "simt": L.PA_KERNE
 
 
 def _vp(t: Optional[torch.Tensor]):
-    return ctypes.c_void_p(t.data_ptr()) if t is not None else ctypes.c_void_p(None)
+    """Device address as a plain int (ctypes converts it for void* parameters)."""
+    return t.data_ptr() if t is not None else None
+
+
+# The current stream's raw handle without building a torch Stream object, which
+# costs a few microseconds per call; the public accessor is the fallback.
+_raw_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None)
 
 
 def _stream(stream: Optional[torch.cuda.Stream]):
-    s = stream if stream is not None else torch.cuda.current_stream()
-    return ctypes.c_void_p(s.cuda_stream)
+    if stream is not None:
+        return stream.cuda_stream
+    if _raw_stream is not None:
+        return _raw_stream(torch.cuda.current_device())
+    return torch.cuda.current_stream().cuda_stream
 
 
 def _need(cond: bool, msg: str):
@@ -44,7 +54,9 @@ def make_cache(k_cache: torch.Tensor, v_cache: torch.Tensor) -> L.PaCache:
     return L.PaCache(k_cache.data_ptr(), v_cache.data_ptr(), hkv, nb, bs, d, _DTYPES[k_cache.dtype])
 
 
+@functools.lru_cache(maxsize=64)
 def _options(split_tokens: int, kernel: str, prefetch: int = 0, warps: int = 0) -> L.PaOptions:
+    """Options struct for these values (cached: libpa only reads it)."""
     return L.PaOptions(int(split_tokens), _KERNELS[kernel], int(prefetch), int(warps))
 
 

@@ -136,6 +136,21 @@ def _nan_fill(shape, dtype: str) -> np.ndarray:
     return np.full(shape, np.nan, dtype=np.float32)
 
 
+def slots_for(block_tables: np.ndarray, context_lens: np.ndarray, num_queries: int,
+              block_size: int = BLOCK_SIZE) -> np.ndarray:
+    """Cache slot of each new token: token i of sequence b sits at position
+    L_b - num_queries + i, in block block_tables[b, pos // block_size]; -1 when
+    that position is negative."""
+    batch = len(context_lens)
+    slots = np.full(batch * num_queries, -1, dtype=np.int32)
+    for b in range(batch):
+        for i in range(num_queries):
+            pos = int(context_lens[b]) - num_queries + i
+            if pos >= 0:
+                slots[b * num_queries + i] = int(block_tables[b, pos // block_size]) * block_size + pos % block_size
+    return slots
+
+
 def generate(spec: Spec, seed: Optional[int] = None) -> Workload:
     """Build one seeded workload from a Spec (see CONFIGS for the five standard ones)."""
     rng = np.random.Generator(np.random.PCG64(spec.seed if seed is None else seed))
@@ -197,12 +212,7 @@ def generate(spec: Spec, seed: Optional[int] = None) -> Workload:
     q = _draw(rng, qshape, spec.dtype)
     k_new = _draw(rng, (spec.batch * nq, hkv, d), spec.dtype)
     v_new = _draw(rng, (spec.batch * nq, hkv, d), spec.dtype)
-    slots = np.full(spec.batch * nq, -1, dtype=np.int32)
-    for b in range(spec.batch):
-        for i in range(nq):
-            pos = int(lens[b]) - nq + i
-            if pos >= 0:
-                slots[b * nq + i] = int(tables[b, pos // bs]) * bs + pos % bs
+    slots = slots_for(tables, lens, nq, bs)
 
     return Workload(spec=spec, k_cache=kc, v_cache=vc, q=q, k_new=k_new, v_new=v_new,
                     slot_mapping=slots, block_tables=tables,

@@ -46,11 +46,12 @@ BF16 = 1
 
 
 def compile_oracle(src: Path, out: Path) -> Path:
-    """Compile one oracle C source into a shared library with gcc (plain -O2, no fast-math)."""
+    """Compile one oracle C source into a shared library with gcc (plain -O2, no fast-math,
+    no fused multiply-add contraction: the int8 quantiser's fp32 steps stay IEEE-exact)."""
     out = Path(out)
     out.parent.mkdir(parents=True, exist_ok=True)
     tmp = out.with_name(out.name + f".tmp{os.getpid()}")
-    cmd = ["gcc", "-O2", "-fopenmp", "-fPIC", "-shared", "-std=c11",
+    cmd = ["gcc", "-O2", "-ffp-contract=off", "-fopenmp", "-fPIC", "-shared", "-std=c11",
            "-o", str(tmp), str(src), "-lm"]
     subprocess.run(cmd, check=True)
     os.replace(tmp, out)
@@ -75,6 +76,10 @@ class Oracle:
         lib.oracle_attend.restype = i32
         lib.oracle_attend.argtypes = [vp, vp, i32, i32, i32, i32, i32, vp, vp, vp, i32, vp,
                                       i32, i32, i32, ctypes.c_double, i32, i32]
+        lib.oracle_cache_write_q8.restype = i32
+        lib.oracle_cache_write_q8.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, vp, vp, vp, i32]
+        lib.oracle_dequant_q8.restype = None
+        lib.oracle_dequant_q8.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, vp, vp]
         lib.oracle_max_threads.restype = i32
         lib.oracle_set_threads.argtypes = [i32]
         self.lib = lib
@@ -151,6 +156,56 @@ class Oracle:
         return self.attend(k_cache, v_cache, q, block_tables, context_lens, scale, b_range)
 
 
+    # ---- int8 cache ("A Rust inference server for Qwen2 on Apple Silicon", Day 4) ----
+
+    def cache_write_q8(self, k_codes: np.ndarray, v_codes: np.ndarray, k_scale: np.ndarray,
+                       v_scale: np.ndarray, k_new: np.ndarray, v_new: np.ndarray,
+                       slot_mapping: np.ndarray) -> int:
+        """In place: quantised write of bf16 rows (see pa_oracle.c, "int8 KV cache").
+
+        Codes [kv_heads, num_blocks, block_size, head_dim] uint8; k_scale
+        [kv_heads, num_blocks, head_dim] float32; v_scale [kv_heads, num_blocks,
+        block_size] float32; new rows [num_tokens, kv_heads, head_dim] uint16 (bf16
+        bits). Returns the count of out-of-range slots.
+        """
+        hkv, nb, bs, d = k_codes.shape
+        assert k_codes.dtype == np.uint8 and v_codes.dtype == np.uint8 and v_codes.shape == k_codes.shape
+        assert k_scale.dtype == np.float32 and k_scale.shape == (hkv, nb, d)
+        assert v_scale.dtype == np.float32 and v_scale.shape == (hkv, nb, bs)
+        n = int(slot_mapping.shape[0])
+        assert k_new.dtype == np.uint16 and k_new.shape == (n, hkv, d) and v_new.shape == k_new.shape
+        slots = np.ascontiguousarray(slot_mapping, dtype=np.int32)
+        return int(self.lib.oracle_cache_write_q8(
+            _ptr(k_codes), _ptr(v_codes), _ptr(k_scale), _ptr(v_scale), hkv, nb, bs, d,
+            _ptr(np.ascontiguousarray(k_new)), _ptr(np.ascontiguousarray(v_new)), _ptr(slots), n))
+
+    def dequant_q8(self, k_codes, v_codes, k_scale, v_scale):
+        """(K, V) as float32 caches of the plain layout: (byte - 128) * scale."""
+        hkv, nb, bs, d = k_codes.shape
+        ko = np.empty((hkv, nb, bs, d), dtype=np.float32)
+        vo = np.empty((hkv, nb, bs, d), dtype=np.float32)
+        self.lib.oracle_dequant_q8(_ptr(np.ascontiguousarray(k_codes)), _ptr(np.ascontiguousarray(v_codes)),
+                                   _ptr(np.ascontiguousarray(k_scale)), _ptr(np.ascontiguousarray(v_scale)),
+                                   hkv, nb, bs, d, _ptr(ko), _ptr(vo))
+        return ko, vo
+
+    def decode_q8(self, k_codes, v_codes, k_scale, v_scale, q, block_tables, context_lens, scale,
+                  b_range=None):
+        """Attention over the dequantised pool (q as bf16 bits, widened exactly)."""
+        ko, vo = self.dequant_q8(k_codes, v_codes, k_scale, v_scale)
+        qf = bf16_bits_to_f64(q).astype(np.float32) if q.dtype == np.uint16 else q.astype(np.float32)
+        return self.attend(ko, vo, qf, block_tables, context_lens, scale, b_range)
+
+    def verify_q8(self, k_codes, v_codes, k_scale, v_scale, q, k_new, v_new, slot_mapping,
+                  block_tables, context_lens, scale, b_range=None):
+        """Quantised write of the new rows (in place), then attention over the pool."""
+        bad = self.cache_write_q8(k_codes, v_codes, k_scale, v_scale, k_new, v_new, slot_mapping)
+        if bad:
+            raise ValueError(f"oracle verify_q8: {bad} out-of-range slot(s)")
+        return self.decode_q8(k_codes, v_codes, k_scale, v_scale, q, block_tables, context_lens,
+                              scale, b_range)
+
+
 def _dtype_code(arr: np.ndarray) -> int:
     if arr.dtype == np.float32:
         return F32
@@ -197,6 +252,22 @@ def decode(*args, **kwargs) -> np.ndarray:
 
 def verify(*args, **kwargs) -> np.ndarray:
     return get().verify(*args, **kwargs)
+
+
+def cache_write_q8(*args, **kwargs) -> int:
+    return get().cache_write_q8(*args, **kwargs)
+
+
+def dequant_q8(*args, **kwargs):
+    return get().dequant_q8(*args, **kwargs)
+
+
+def decode_q8(*args, **kwargs) -> np.ndarray:
+    return get().decode_q8(*args, **kwargs)
+
+
+def verify_q8(*args, **kwargs) -> np.ndarray:
+    return get().verify_q8(*args, **kwargs)
 
 
 def bf16_bits_to_f64(bits: np.ndarray) -> np.ndarray:

@@ -214,3 +214,141 @@ int oracle_attend(const void *k_cache, const void *v_cache, int dtype,
     }
     return bad;
 }
+
+/*
+ * int8 KV cache ("A Rust inference server for Qwen2 on Apple Silicon",
+ * Day 4 measurements, sections "int8 KV", "Grouping is the whole question"
+ * and "Partial blocks").
+ *
+ *  - Codes. Symmetric int8 values q in [-127, 127], stored as the byte
+ *    q + 128 (the page keeps u8 with a +128 offset).
+ *  - Groups. K is scaled per channel within a block: one scale per (kv head,
+ *    block, channel), spanning the block's rows. V is scaled per token: one
+ *    scale per (kv head, block, row). This is the KIVI grouping the page
+ *    adopts.
+ *  - Quantising a group is done in fp32, the precision of the page's
+ *    tensors: s = max |x| / 127, and q = x / s rounded to nearest (reading:
+ *    the page names no rounding; this takes IEEE's default, ties to even),
+ *    clamped to [-127, 127]. An all-zero group gets s = 0 and bytes 128
+ *    (reading: the page is silent on it).
+ *  - Dequantising is one fp32 multiply: x = (byte - 128) * s.
+ *  - Writing rows ("Partial blocks"). For each block that receives rows in a
+ *    call, the block's K rows are dequantised, the incoming rows overwrite
+ *    theirs, every channel's scale is recomputed over the block's rows, and
+ *    all rows are requantised. Each incoming V row is quantised on its own.
+ *    Rows never written hold byte 128 (zero), so they cannot raise a maximum.
+ *    (Reading: all rows one call writes into a block are overwritten
+ *    together before the block's single requantisation; with duplicate slots
+ *    the later token wins, as in the plain write.)
+ *
+ * New rows arrive as bf16 bit patterns and widen to fp32 exactly.
+ */
+
+static float q8_widen_bf16(uint16_t bits) {
+    const uint32_t u = (uint32_t)bits << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return f;
+}
+
+/* Scale of a group whose largest magnitude is maxabs. */
+static float q8_scale(float maxabs) { return maxabs / 127.0f; }
+
+/* Stored byte of value x in a group of scale s. */
+static uint8_t q8_code(float x, float s) {
+    if (s == 0.0f) return 128;
+    float r = rintf(x / s);
+    if (r > 127.0f) r = 127.0f;
+    if (r < -127.0f) r = -127.0f;
+    return (uint8_t)((int)r + 128);
+}
+
+static float q8_value(uint8_t byte, float s) { return (float)((int)byte - 128) * s; }
+
+/*
+ * Quantised slot-mapping write. Codes: [kv_heads, num_blocks, block_size,
+ * head_dim] bytes; k_scale: [kv_heads, num_blocks, head_dim] fp32; v_scale:
+ * [kv_heads, num_blocks, block_size] fp32. k_new / v_new: [num_tokens,
+ * kv_heads, head_dim] bf16 bits. Negative slots are skipped; out-of-range
+ * slots are skipped and counted (the return value).
+ */
+int oracle_cache_write_q8(uint8_t *k_codes, uint8_t *v_codes, float *k_scale, float *v_scale,
+                          int kv_heads, int num_blocks, int block_size, int head_dim,
+                          const uint16_t *k_new, const uint16_t *v_new,
+                          const int32_t *slot_mapping, int num_tokens) {
+    const int64_t num_slots = (int64_t)num_blocks * block_size;
+    int out_of_range = 0;
+    float *x = (float *)malloc((size_t)block_size * head_dim * sizeof(float));
+    for (int i = 0; i < num_tokens; ++i) {
+        const int64_t slot = slot_mapping[i];
+        if (slot < 0) continue;
+        if (slot >= num_slots) {
+            ++out_of_range;
+            continue;
+        }
+        const int64_t block = slot / block_size;
+        /* The block is handled once, at the first token of this call that lands in it. */
+        int seen = 0;
+        for (int j = 0; j < i; ++j) {
+            const int64_t sj = slot_mapping[j];
+            if (sj >= 0 && sj < num_slots && sj / block_size == block) seen = 1;
+        }
+        if (seen) continue;
+        for (int h = 0; h < kv_heads; ++h) {
+            const int64_t blk = (int64_t)h * num_blocks + block;
+            uint8_t *kc = k_codes + blk * block_size * head_dim;
+            float *ks = k_scale + blk * head_dim;
+            /* K: dequantise the block, overwrite the incoming rows, requantise per channel. */
+            for (int r = 0; r < block_size; ++r)
+                for (int d = 0; d < head_dim; ++d)
+                    x[r * head_dim + d] = q8_value(kc[r * head_dim + d], ks[d]);
+            for (int j = i; j < num_tokens; ++j) {
+                const int64_t sj = slot_mapping[j];
+                if (sj < 0 || sj >= num_slots || sj / block_size != block) continue;
+                const int r = (int)(sj % block_size);
+                const uint16_t *src = k_new + ((int64_t)j * kv_heads + h) * head_dim;
+                for (int d = 0; d < head_dim; ++d) x[r * head_dim + d] = q8_widen_bf16(src[d]);
+            }
+            for (int d = 0; d < head_dim; ++d) {
+                float m = 0.0f;
+                for (int r = 0; r < block_size; ++r) {
+                    const float a = fabsf(x[r * head_dim + d]);
+                    if (a > m) m = a;
+                }
+                ks[d] = q8_scale(m);
+                for (int r = 0; r < block_size; ++r) kc[r * head_dim + d] = q8_code(x[r * head_dim + d], ks[d]);
+            }
+            /* V: each incoming row on its own scale. */
+            for (int j = i; j < num_tokens; ++j) {
+                const int64_t sj = slot_mapping[j];
+                if (sj < 0 || sj >= num_slots || sj / block_size != block) continue;
+                const int r = (int)(sj % block_size);
+                const uint16_t *src = v_new + ((int64_t)j * kv_heads + h) * head_dim;
+                float m = 0.0f;
+                for (int d = 0; d < head_dim; ++d) {
+                    const float a = fabsf(q8_widen_bf16(src[d]));
+                    if (a > m) m = a;
+                }
+                const float s = q8_scale(m);
+                v_scale[blk * block_size + r] = s;
+                uint8_t *vc = v_codes + (blk * block_size + r) * head_dim;
+                for (int d = 0; d < head_dim; ++d) vc[d] = q8_code(q8_widen_bf16(src[d]), s);
+            }
+        }
+    }
+    free(x);
+    return out_of_range;
+}
+
+/* Dequantise a whole pool into fp32 caches of the plain layout. */
+void oracle_dequant_q8(const uint8_t *k_codes, const uint8_t *v_codes, const float *k_scale,
+                       const float *v_scale, int kv_heads, int num_blocks, int block_size,
+                       int head_dim, float *k_out, float *v_out) {
+    for (int64_t blk = 0; blk < (int64_t)kv_heads * num_blocks; ++blk)
+        for (int r = 0; r < block_size; ++r)
+            for (int d = 0; d < head_dim; ++d) {
+                const int64_t e = (blk * block_size + r) * head_dim + d;
+                k_out[e] = q8_value(k_codes[e], k_scale[blk * head_dim + d]);
+                v_out[e] = q8_value(v_codes[e], v_scale[blk * block_size + r]);
+            }
+}

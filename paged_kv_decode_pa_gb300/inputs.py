@@ -237,3 +237,44 @@ def custom(batch: int, q_heads: int, kv_heads: int, context_lens, num_blocks: in
                 num_queries=num_queries, spare_block=spare_block, padded_rows=padded_rows,
                 head_dim=head_dim, block_size=block_size)
     return generate(spec)
+
+
+@dataclass
+class Q8Pool:
+    """An int8 KV pool: bytes (value + 128) with K scales per (head, block,
+    channel) and V scales per (head, block, row)."""
+    k_codes: np.ndarray   # [kv_heads, num_blocks, block_size, head_dim] uint8
+    v_codes: np.ndarray
+    k_scale: np.ndarray   # [kv_heads, num_blocks, head_dim] float32
+    v_scale: np.ndarray   # [kv_heads, num_blocks, block_size] float32
+
+
+def q8_pool(w: Workload, seed: Optional[int] = None) -> Q8Pool:
+    """A seeded int8 pool for a workload's tables and lengths.
+
+    Every row a sequence holds (and the spare block's rows) gets bell-shaped
+    bytes (a rounded N(0, 1) x 42 draw, clipped to [1, 255]); every other row
+    holds byte 128, a zero. K scales are drawn from U(0.005, 0.05) for every
+    (head, block, channel); V scales likewise for held rows and NaN for the
+    rest, so a read of a row no sequence holds shows up. Draws only: no
+    quantiser runs here.
+    """
+    s = w.spec
+    rng = np.random.Generator(np.random.PCG64((s.seed if seed is None else seed) + 7919))
+    hkv, nb, bs, d = s.kv_heads, s.num_blocks, s.block_size, s.head_dim
+    held = np.zeros((nb, bs), dtype=bool)
+    for b in range(w.real_rows):
+        t = np.arange(int(w.context_lens[b]))
+        held[w.block_tables[b, t // bs], t % bs] = True
+    if w.spare_block is not None:
+        held[w.spare_block, :] = True
+    def codes():
+        c = np.full((hkv, nb, bs, d), 128, dtype=np.uint8)
+        draw = np.clip(np.rint(rng.standard_normal((hkv, int(held.sum()), d)) * 42.0), -127, 127)
+        c[:, held, :] = (draw + 128).astype(np.uint8)
+        return c
+    kq, vq = codes(), codes()
+    ks = rng.uniform(0.005, 0.05, size=(hkv, nb, d)).astype(np.float32)
+    vs = np.full((hkv, nb, bs), np.nan, dtype=np.float32)
+    vs[:, held] = rng.uniform(0.005, 0.05, size=(hkv, int(held.sum()))).astype(np.float32)
+    return Q8Pool(kq, vq, ks, vs)

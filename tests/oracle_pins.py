@@ -18,7 +18,11 @@ AssertionError when the oracle disagrees with an independent fact:
 * the verify rows' causal reading: row i of a verify step equals a decode
   whose context ends at that row's position;
 * the cache write: a numpy fancy-index scatter, with every other byte of the
-  pool unchanged.
+  pool unchanged;
+* the int8 pool: hand-worked codes and scales (ties to even, the +128
+  offset), the requantisation of a block when a channel's maximum grows,
+  order independence on the quantisation grid, the half-step error bound, and
+  lossless grid values giving attention bit-identical to the bf16 pool.
 
 Run as a script with a library path, it executes every pin against that
 library and exits non-zero if any pin fails (used by the mutation test, which
@@ -272,9 +276,164 @@ def pin_cache_write(orc):
         assert orc.cache_write(kc, vc, w.k_new, w.v_new, big) == 1
 
 
+# ---------------------------------------------------------------------------
+# int8 pool ("A Rust inference server for Qwen2 on Apple Silicon", Day 4:
+# "int8 KV", "Grouping is the whole question", "Partial blocks").
+
+def _bf16(x):
+    """float values -> bf16 bit patterns (the values used here are bf16-exact)."""
+    f = np.asarray(x, dtype=np.float32)
+    bits = f.view(np.uint32)
+    assert np.all(bits & 0xFFFF == 0), "pin values must be exact in bf16"
+    return (bits >> 16).astype(np.uint16)
+
+
+def _empty_q8(hkv, nb, bs=16, d=128):
+    """A pool no row was ever written to: byte 128 (zero) everywhere, zero scales."""
+    return (np.full((hkv, nb, bs, d), 128, np.uint8), np.full((hkv, nb, bs, d), 128, np.uint8),
+            np.zeros((hkv, nb, d), np.float32), np.zeros((hkv, nb, bs), np.float32))
+
+
+def _q8_row(d=128):
+    """One row with hand-checked codes at scale 15.875 / 127 = 1/8 (exact)."""
+    v = np.zeros(d, np.float32)
+    v[:8] = [15.875, -15.875, 0.0, 7.9375, 7.8125, -7.8125, 0.0625, 0.1875]
+    # x / (1/8) = 127, -127, 0, 63.5, 62.5, -62.5, 0.5, 1.5 -> ties go to even.
+    want = np.full(d, 128, np.uint8)
+    want[:8] = [255, 1, 128, 192, 190, 66, 128, 130]
+    return v, want
+
+
+def pin_q8_row_closed_form(orc):
+    """One token into an empty block: V gets the row's own scale and the codes
+    worked out by hand (round to nearest, ties to even, +128 offset); each K
+    channel's scale is |k| / 127 (the row is the only non-zero one), its code
+    +-127, and every other row stays byte 128."""
+    kq, vq, ks, vs = _empty_q8(1, 2)
+    v, want = _q8_row()
+    row = _bf16(v)[None, None, :]
+    assert orc.cache_write_q8(kq, vq, ks, vs, row, row, np.array([16 + 5], np.int32)) == 0
+    assert vs[0, 1, 5] == np.float32(0.125)
+    assert np.array_equal(vq[0, 1, 5], want)
+    nz = v != 0
+    assert np.array_equal(ks[0, 1][nz], np.abs(v[nz]) / np.float32(127)) and np.all(ks[0, 1][~nz] == 0)
+    assert np.array_equal(kq[0, 1, 5][nz], np.where(v[nz] > 0, 255, 1).astype(np.uint8))
+    assert np.all(kq[0, 1, 5][~nz] == 128)
+    others = np.ones(16, bool)
+    others[5] = False
+    assert np.all(kq[0, 1][others] == 128) and np.all(vq[0, 1][others] == 128) and np.all(vs[0, 1][others] == 0)
+    assert np.all(kq[0, 0] == 128) and np.all(ks[0, 0] == 0)  # the other block is untouched
+
+
+def pin_q8_requant_closed_form(orc):
+    """A later, larger value in a channel re-scales that channel for the whole
+    block (the old row's code is recomputed at the new scale), and a channel
+    whose maximum did not change keeps its codes exactly."""
+    kq, vq, ks, vs = _empty_q8(1, 1)
+    a = np.zeros(128, np.float32)
+    a[0] = a[1] = 15.875
+    b = np.zeros(128, np.float32)
+    b[0], b[1] = 31.75, 1.0
+    orc.cache_write_q8(kq, vq, ks, vs, _bf16(a)[None, None], _bf16(a)[None, None], np.array([0], np.int32))
+    assert ks[0, 0, 0] == 0.125 and kq[0, 0, 0, 0] == 255
+    orc.cache_write_q8(kq, vq, ks, vs, _bf16(b)[None, None], _bf16(b)[None, None], np.array([1], np.int32))
+    assert ks[0, 0, 0] == 0.25 and ks[0, 0, 1] == 0.125
+    assert kq[0, 0, 0, 0] == 192  # 15.875 / 0.25 = 63.5 -> 64
+    assert kq[0, 0, 1, 0] == 255 and kq[0, 0, 0, 1] == 255 and kq[0, 0, 1, 1] == 136  # 1 / 0.125 = 8
+    # V rows are independent: the first row's V is untouched by the second write.
+    assert vs[0, 0, 0] == 0.125 and vs[0, 0, 1] == 0.25 and vq[0, 0, 0, 0] == 255
+
+
+def pin_q8_zero_and_partial_block(orc):
+    """An all-zero row has scale 0, bytes 128 and dequantises to 0. Rows on the
+    quantisation grid fill a block to the same bytes whether they come one per
+    call or all in one call: unwritten rows are zeros and cannot raise a
+    maximum, and requantising at an unchanged scale returns each code."""
+    kq, vq, ks, vs = _empty_q8(1, 1)
+    z = np.zeros((1, 1, 128), np.uint16)
+    orc.cache_write_q8(kq, vq, ks, vs, z, z, np.array([3], np.int32))
+    assert vs[0, 0, 3] == 0 and np.all(vq[0, 0, 3] == 128) and np.all(ks == 0)
+    ko, vo = orc.dequant_q8(kq, vq, ks, vs)
+    assert np.all(ko == 0) and np.all(vo == 0)
+
+    rng = np.random.default_rng(11)
+    ints = rng.integers(-126, 127, size=(4, 128))
+    ints[0] = np.where(rng.random(128) < 0.5, 127, -127)  # row 0 holds every channel's maximum
+    rows = _bf16(ints.astype(np.float32) / 8)[:, None, :]
+    one = _empty_q8(1, 1)
+    orc.cache_write_q8(*one, rows, rows, np.arange(4, dtype=np.int32))
+    step = _empty_q8(1, 1)
+    for r in range(4):
+        orc.cache_write_q8(*step, rows[r:r + 1], rows[r:r + 1], np.array([r], np.int32))
+    for x, y in zip(one, step):
+        assert np.array_equal(x, y)
+    assert np.array_equal(one[0][0, 0, :4], (ints + 128).astype(np.uint8))  # lossless on the grid
+
+
+def pin_q8_error_bound(orc):
+    """Every dequantised element is within half a step of its bf16 input: the
+    error is about scale / 2 per element ("Grouping is the whole question")."""
+    rng = np.random.default_rng(12)
+    n, hkv = 40, 2
+    vals = (rng.standard_normal((n, hkv, 128)) * rng.uniform(0.1, 8, size=(n, 1, 1))).astype(np.float32)
+    vals = ((vals.view(np.uint32) + 0x8000) & 0xFFFF0000).view(np.float32)  # to bf16 values
+    k_new, v_new = _bf16(vals), _bf16(vals[::-1].copy())
+    slots = rng.permutation(4 * 16)[:n].astype(np.int32)  # several rows per block
+    kq, vq, ks, vs = _empty_q8(hkv, 4)
+    assert orc.cache_write_q8(kq, vq, ks, vs, k_new, v_new, slots) == 0
+    ko, vo = orc.dequant_q8(kq, vq, ks, vs)
+    xk = np.zeros((hkv, 4, 16, 128), np.float32)
+    xv = np.zeros((hkv, 4, 16, 128), np.float32)
+    xk[:, slots // 16, slots % 16] = vals.transpose(1, 0, 2)
+    xv[:, slots // 16, slots % 16] = vals[::-1].transpose(1, 0, 2)
+    sk = np.abs(xk).max(axis=2, keepdims=True) / 127  # per channel over the block's rows
+    sv = np.abs(xv).max(axis=3, keepdims=True) / 127  # per row
+    assert np.all(np.abs(ko.astype(np.float64) - xk) <= sk * (0.5 + 1e-5))
+    assert np.all(np.abs(vo.astype(np.float64) - xv) <= sv * (0.5 + 1e-5))
+    big = slots.copy()
+    big[0] = 4 * 16
+    assert orc.cache_write_q8(*_empty_q8(hkv, 4), k_new, v_new, big) == 1
+
+
+def pin_q8_lossless_attention(orc):
+    """Values already on the quantisation grid survive the int8 pool exactly, so
+    attention over the pool equals the pinned attention over the same values
+    held as bf16, bit for bit."""
+    rng = np.random.default_rng(13)
+    hkv, hq, bs, nb = 2, 6, 16, 12
+    lens = np.array([1, 16, 37, 70], np.int32)
+    tables = np.zeros((4, 5), np.int32)
+    perm = rng.permutation(nb)
+    cur = 0
+    for b, L in enumerate(lens):
+        n = -(-int(L) // bs)
+        tables[b, :n] = perm[cur:cur + n]
+        cur += n
+    slots = np.concatenate([tables[b, np.arange(L) // bs] * bs + np.arange(L) % bs for b, L in enumerate(lens)])
+    n = slots.size
+    ki = np.clip(np.rint(rng.standard_normal((n, hkv, 128)) * 30), -126, 126)
+    vi = np.clip(np.rint(rng.standard_normal((n, hkv, 128)) * 30), -126, 126)
+    # K: in every block and channel one written row reaches 127; V: every row reaches 127.
+    for blk in np.unique(slots // bs):
+        first = np.nonzero(slots // bs == blk)[0][0]
+        ki[first] = np.where(rng.random((hkv, 128)) < 0.5, 127, -127)
+    vi[:, :, 0] = np.where(rng.random((n, hkv)) < 0.5, 127, -127)
+    kb, vb = _bf16(ki / 16), _bf16(vi / 16)
+    pool = _empty_q8(hkv, nb)
+    assert orc.cache_write_q8(*pool, kb, vb, slots.astype(np.int32)) == 0
+    kc = np.zeros((hkv, nb, bs, 128), np.uint16)
+    vc = np.zeros((hkv, nb, bs, 128), np.uint16)
+    assert orc.cache_write(kc, vc, kb, vb, slots.astype(np.int32)) == 0
+    q = _bf16(((rng.standard_normal((4, 1, hq, 128)).astype(np.float32).view(np.uint32)) & 0xFFFF0000).view(np.float32))
+    got = orc.decode_q8(*pool, q, tables, lens, 1 / np.sqrt(128))
+    ref = orc.attend(kc, vc, q, tables, lens, 1 / np.sqrt(128))
+    assert np.array_equal(got, ref)
+
+
 ALL_PINS = [pin_bruteforce, pin_sdpa, pin_onehot_softmax, pin_constant_v, pin_single_token,
             pin_two_token_closed_form, pin_block_permutation, pin_gqa_repeat, pin_verify_rows,
-            pin_zero_length, pin_cache_write]
+            pin_zero_length, pin_cache_write, pin_q8_row_closed_form, pin_q8_requant_closed_form,
+            pin_q8_zero_and_partial_block, pin_q8_error_bound, pin_q8_lossless_attention]
 
 
 if __name__ == "__main__":

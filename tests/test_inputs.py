@@ -56,3 +56,22 @@ def test_padded_rows_only_touch_the_spare_block():
     assert np.all(w.block_tables[57:] == w.spare_block)
     assert np.all((w.context_lens[57:] >= 1) & (w.context_lens[57:] <= 16))
     assert np.all(w.slot_mapping[57:] // 16 == w.spare_block)
+
+
+def test_q8_pool_structure():
+    """The int8 pool generator: held rows get drawn bytes in [1, 255] and finite
+    V scales; other rows hold byte 128 with NaN V scales; K scales are finite."""
+    w = inputs.make("c3")
+    p = inputs.q8_pool(w)
+    hkv, nb, bs, d = p.k_codes.shape
+    assert p.k_scale.shape == (hkv, nb, d) and p.v_scale.shape == (hkv, nb, bs)
+    held = np.zeros((nb, bs), bool)
+    for b in range(w.real_rows):
+        t = np.arange(int(w.context_lens[b]))
+        held[w.block_tables[b, t // bs], t % bs] = True
+    held[w.spare_block] = True
+    assert np.all(p.k_codes[:, ~held] == 128) and np.all(p.v_codes[:, ~held] == 128)
+    assert p.k_codes[:, held].min() >= 1 and np.isfinite(p.v_scale[:, held]).all()
+    assert np.isnan(p.v_scale[:, ~held]).all() and np.isfinite(p.k_scale).all()
+    again = inputs.q8_pool(w)
+    assert np.array_equal(again.k_codes, p.k_codes) and np.array_equal(again.v_scale, p.v_scale, equal_nan=True)

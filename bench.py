@@ -216,18 +216,27 @@ class DecodeStep:
     the two calls. A verify workload's step is pa_verify.
     """
 
-    def __init__(self, w, device, split_tokens=0, kernel="auto", prefetch=0, warps=0, fused=True):
+    def __init__(self, w, device, split_tokens=0, kernel="auto", prefetch=0, warps=0, fused=True, kv="bf16"):
         import paged_kv_decode_pa_gb300 as pa
 
         self.pa = pa
         self.w = w
+        self.kv = kv
         self.dev = device
         self.split = split_tokens
         self.kernel = kernel
         self.prefetch = prefetch
         self.warps = warps
-        self.kc = pa.to_torch(w.k_cache, device)
-        self.vc = pa.to_torch(w.v_cache, device)
+        self.scales = {}
+        if kv == "int8":  # a seeded int8 pool for the same tables and lengths
+            pool = inputs.q8_pool(w)
+            self.kc = pa.to_torch(pool.k_codes, device)
+            self.vc = pa.to_torch(pool.v_codes, device)
+            self.scales = {"k_scale": pa.to_torch(pool.k_scale, device),
+                           "v_scale": pa.to_torch(pool.v_scale, device)}
+        else:
+            self.kc = pa.to_torch(w.k_cache, device)
+            self.vc = pa.to_torch(w.v_cache, device)
         self.q = pa.to_torch(w.q, device)
         self.k_new = pa.to_torch(w.k_new, device)
         self.v_new = pa.to_torch(w.v_new, device)
@@ -254,19 +263,19 @@ class DecodeStep:
         return st
 
     def write(self):
-        self.pa.pa_cache_write(self.kc, self.vc, self.k_new, self.v_new, self.slots)
+        self.pa.pa_cache_write(self.kc, self.vc, self.k_new, self.v_new, self.slots, **self.scales)
 
     def attend(self):
         w = self.w
         if not self.fused:
             self.pa.pa_decode(self.kc, self.vc, self.q, self.tables, self.lens, w.max_context_len, w.scale,
                               self.ws, out=self.out, split_tokens=self.split, kernel=self.kernel,
-                              prefetch=self.prefetch, warps=self.warps)
+                              prefetch=self.prefetch, warps=self.warps, **self.scales)
         else:
             self.pa.pa_verify(self.kc, self.vc, self.q4, self.k_new, self.v_new, self.slots, self.tables,
                               self.lens, w.max_context_len, w.scale, self.ws, out=self.out4,
                               split_tokens=self.split, kernel=self.kernel, prefetch=self.prefetch,
-                              warps=self.warps)
+                              warps=self.warps, **self.scales)
 
     def run(self):
         """One whole step."""
@@ -407,21 +416,26 @@ def time_e2e(step: DecodeStep, steps: int, warmup: int, flush):
     return [e[0].elapsed_time(e[1]) for e in ev], h2d, d2h
 
 
-def step_bytes(w, fused=True):
+def step_bytes(w, fused=True, kv="bf16"):
     s = w.spec
     eb = accounting.elem_bytes(s.dtype)
     fused_write = fused or s.num_queries > 1
+    if kv == "int8":
+        att = accounting.decode_bytes_q8(w.context_lens, s.q_heads, s.kv_heads, s.head_dim, s.num_queries,
+                                         fused_write=fused_write)
+        return att, 0
     att = accounting.decode_bytes(w.context_lens, s.q_heads, s.kv_heads, s.head_dim, eb, s.num_queries,
                                   fused_write=fused_write)
     write = 0 if fused_write else accounting.cache_write_bytes(len(w.slot_mapping), s.kv_heads, s.head_dim, eb)
     return att, write
 
 
-def measure_extra(name, device, steps, flush, split, kernel, prefetch=0, warps=0, fused=True, graph=False):
+def measure_extra(name, device, steps, flush, split, kernel, prefetch=0, warps=0, fused=True, graph=False,
+                  kv="bf16"):
     w = inputs.make(name)
-    st = DecodeStep(w, device, split, kernel, prefetch, warps, fused)
+    st = DecodeStep(w, device, split, kernel, prefetch, warps, fused, kv)
     total, attend = time_steps(st, steps, 3, flush, graph)
-    att, _ = step_bytes(w, fused)
+    att, _ = step_bytes(w, fused, kv)
     us = statistics.mean(attend) * 1e3
     peak, _ = hbm_peak()
     gbs = att["total"] / (us * 1e-6) / 1e9
@@ -434,7 +448,7 @@ def measure_extra(name, device, steps, flush, split, kernel, prefetch=0, warps=0
            "us_per_call_median": round(statistics.median(attend) * 1e3, 2),
            "call": ("pa_verify (fused write)" if w.spec.num_queries > 1 else
                     "pa_verify, one query per sequence (fused append + decode)" if fused else "pa_decode"),
-           "l2": "flushed (write + read) before each call"}
+           "l2": "flushed (write + read) before each call", "kv": kv}
     # Warm variant: no flush between calls, so whatever of the working set
     # fits in L2 (129 MB) is read from there.
     _, warm = time_steps(st, steps, 3, lambda: None, graph)
@@ -488,6 +502,11 @@ def run_native(args):
             if name != args.workload:
                 extra[name] = measure_extra(name, device, 20, flush, args.split_tokens, args.kernel,
                                             args.prefetch, args.warps, not args.unfused, args.graph)
+        # The int8 pool (the next row of the scope): the same workloads with
+        # dequantisation fused into the attention kernel.
+        for name in ("c4", "c3", "c5"):
+            extra[name + "_int8"] = measure_extra(name, device, 20, flush, args.split_tokens, "auto", 0, 0,
+                                                  not args.unfused, args.graph, kv="int8")
 
     cpu = cpu_baseline(w, args.cpu_seconds) if rank == 0 else None
 

@@ -51,8 +51,23 @@
  *  - Kernels contain no trap and no unbounded wait. A wait that exceeds its
  *    limit raises PA_FLAG_TIMEOUT and the kernel returns.
  *
- * Supported shapes: head_dim 128, block_size 16, dtype bf16 or fp32,
+ * Supported shapes: head_dim 128, block_size 16, dtype bf16, fp32 or int8,
  * q_heads a multiple of kv_heads.
+ *
+ * The int8 pool ("A Rust inference server for Qwen2 on Apple Silicon", Day 4
+ * "int8 KV", "Grouping is the whole question", "Partial blocks"):
+ *  - k and v hold bytes q + 128 of symmetric codes q in [-127, 127], in the
+ *    same head-major layout. k_scale holds one fp32 scale per (kv head,
+ *    block, channel), [kv_heads, num_blocks, head_dim]. v_scale holds one per
+ *    (kv head, block, row), [kv_heads, num_blocks, block_size].
+ *  - A stored value is (byte - 128) * scale.
+ *  - Quantising a group takes s = max|x| / 127 and q = x / s rounded to
+ *    nearest, ties to even, in fp32 with IEEE division. An all-zero group
+ *    has s = 0 and bytes 128.
+ *  - Queries, new rows and outputs are bf16. Attention dequantises inside
+ *    the kernel. K values enter the products rounded to f16; V bytes enter
+ *    exactly, with the row scales folded into the softmax weights. K values
+ *    must stay below 65504 in magnitude.
  */
 #ifndef PA_H_
 #define PA_H_
@@ -64,10 +79,12 @@
 extern "C" {
 #endif
 
-/* Element type of caches, queries, new rows and outputs (all the same). */
+/* Element type of the caches. For F32 and BF16, queries, new rows and
+ * outputs have the same type; for INT8 they are bf16. */
 typedef enum pa_dtype {
     PA_DTYPE_F32 = 0,
-    PA_DTYPE_BF16 = 1
+    PA_DTYPE_BF16 = 1,
+    PA_DTYPE_INT8 = 2
 } pa_dtype;
 
 typedef enum pa_status {
@@ -94,6 +111,11 @@ typedef struct pa_cache {
     int32_t block_size; /* must be 16 */
     int32_t head_dim;   /* must be 128 */
     int32_t dtype;      /* pa_dtype */
+    /* PA_DTYPE_INT8 only (ignored otherwise): fp32 scales, device, 16-byte
+     * aligned. k_scale [kv_heads, num_blocks, head_dim]; v_scale [kv_heads,
+     * num_blocks, block_size]. */
+    void *k_scale;
+    void *v_scale;
 } pa_cache;
 
 /* Kernel choice for pa_decode / pa_verify. */
@@ -137,11 +159,18 @@ typedef struct pa_options {
  * Stall", the engine's Model._layer).
  *
  *   cache         the pool (device tensors written in place).
- *   d_k_new, d_v_new  [num_tokens, kv_heads, head_dim] of cache->dtype, device.
+ *   d_k_new, d_v_new  [num_tokens, kv_heads, head_dim] of cache->dtype (bf16
+ *                     for an int8 pool), device.
  *   d_slot_mapping    [num_tokens] int32, device. s < 0: token skipped.
  *                     s >= num_blocks*16: skipped (no status word here; use
  *                     pa_validate to find it). Duplicate slots: unspecified
- *                     which write lands.
+ *                     which write lands (int8: the later token).
+ *
+ * int8 pool: the write quantises ("Partial blocks" of the int8 page). For
+ * every block that receives rows in this call, its K rows are dequantised,
+ * the incoming rows overwrite theirs, each channel's scale is recomputed over
+ * the block and every row is requantised. Each incoming V row is quantised
+ * on its own scale. Bytes and scales are deterministic (exact fp32 steps).
  *   num_tokens    >= 0; 0 launches nothing.
  *   stream        cudaStream_t (NULL = legacy default stream).
  * Returns PA_OK or an error status (nothing launched on error).
@@ -209,6 +238,12 @@ pa_status pa_decode(const pa_cache *cache, const void *d_q, void *d_out,
  * this); the attention reads the new rows from d_k_new / d_v_new directly.
  * A row whose position is negative returns zeros. Padded query rows are
  * computed like any other and may be discarded by the caller.
+ *
+ * int8 pool: the call runs the quantised pa_cache_write, then the attention
+ * kernel as its programmatic dependent. That kernel streams the blocks
+ * before the new tokens at once, and waits for the write only before the
+ * blocks that hold them. The result equals pa_cache_write followed by
+ * pa_decode-style attention over the requantised pool, for any slots.
  *
  *   d_q, d_out     [batch, num_queries, q_heads, head_dim], device.
  *   d_k_new, d_v_new [batch * num_queries, kv_heads, head_dim], device.

@@ -227,10 +227,13 @@ int oracle_attend(const void *k_cache, const void *v_cache, int dtype,
  *    scale per (kv head, block, row). This is the KIVI grouping the page
  *    adopts.
  *  - Quantising a group is done in fp32, the precision of the page's
- *    tensors: s = max |x| / 127, and q = x / s rounded to nearest (reading:
- *    the page names no rounding; this takes IEEE's default, ties to even),
- *    clamped to [-127, 127]. An all-zero group gets s = 0 and bytes 128
- *    (reading: the page is silent on it).
+ *    tensors. The stored scale is s = max |x| / 127, and q = x * (127 / max|x|)
+ *    rounded to nearest, clamped to [-127, 127]. (Reading: the page fixes
+ *    the scale by the group's largest magnitude but not how a code is
+ *    rounded; this takes the usual quantiser form, one inverse scale per
+ *    group and a multiply per element, rounded with IEEE's default, ties to
+ *    even.) An all-zero group gets s = 0 and bytes 128 (reading: the page is
+ *    silent on it).
  *  - Dequantising is one fp32 multiply: x = (byte - 128) * s.
  *  - Writing rows ("Partial blocks"). For each block that receives rows in a
  *    call, the block's K rows are dequantised, the incoming rows overwrite
@@ -254,10 +257,13 @@ static float q8_widen_bf16(uint16_t bits) {
 /* Scale of a group whose largest magnitude is maxabs. */
 static float q8_scale(float maxabs) { return maxabs / 127.0f; }
 
-/* Stored byte of value x in a group of scale s. */
-static uint8_t q8_code(float x, float s) {
-    if (s == 0.0f) return 128;
-    float r = rintf(x / s);
+/* Inverse scale used to quantise that group (0 for an all-zero group). */
+static float q8_inverse(float maxabs) { return maxabs == 0.0f ? 0.0f : 127.0f / maxabs; }
+
+/* Stored byte of value x in a group of inverse scale inv. */
+static uint8_t q8_code(float x, float inv) {
+    if (inv == 0.0f) return 128;
+    float r = rintf(x * inv);
     if (r > 127.0f) r = 127.0f;
     if (r < -127.0f) r = -127.0f;
     return (uint8_t)((int)r + 128);
@@ -316,7 +322,8 @@ int oracle_cache_write_q8(uint8_t *k_codes, uint8_t *v_codes, float *k_scale, fl
                     if (a > m) m = a;
                 }
                 ks[d] = q8_scale(m);
-                for (int r = 0; r < block_size; ++r) kc[r * head_dim + d] = q8_code(x[r * head_dim + d], ks[d]);
+                const float inv = q8_inverse(m);
+                for (int r = 0; r < block_size; ++r) kc[r * head_dim + d] = q8_code(x[r * head_dim + d], inv);
             }
             /* V: each incoming row on its own scale. */
             for (int j = i; j < num_tokens; ++j) {
@@ -329,10 +336,10 @@ int oracle_cache_write_q8(uint8_t *k_codes, uint8_t *v_codes, float *k_scale, fl
                     const float a = fabsf(q8_widen_bf16(src[d]));
                     if (a > m) m = a;
                 }
-                const float s = q8_scale(m);
-                v_scale[blk * block_size + r] = s;
+                v_scale[blk * block_size + r] = q8_scale(m);
+                const float inv = q8_inverse(m);
                 uint8_t *vc = v_codes + (blk * block_size + r) * head_dim;
-                for (int d = 0; d < head_dim; ++d) vc[d] = q8_code(q8_widen_bf16(src[d]), s);
+                for (int d = 0; d < head_dim; ++d) vc[d] = q8_code(q8_widen_bf16(src[d]), inv);
             }
         }
     }

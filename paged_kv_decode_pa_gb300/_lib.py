@@ -19,6 +19,7 @@ PA_ERR_CUDA = 4
 
 PA_DTYPE_F32 = 0
 PA_DTYPE_BF16 = 1
+PA_DTYPE_INT8 = 2
 
 PA_KERNEL_AUTO = 0
 PA_KERNEL_MMA = 1
@@ -45,7 +46,8 @@ EXPORTED = ("pa_cache_write", "pa_workspace_size", "pa_workspace_init", "pa_work
 class PaCache(ctypes.Structure):
     _fields_ = [("k", ctypes.c_void_p), ("v", ctypes.c_void_p), ("kv_heads", ctypes.c_int32),
                 ("num_blocks", ctypes.c_int32), ("block_size", ctypes.c_int32),
-                ("head_dim", ctypes.c_int32), ("dtype", ctypes.c_int32)]
+                ("head_dim", ctypes.c_int32), ("dtype", ctypes.c_int32),
+                ("k_scale", ctypes.c_void_p), ("v_scale", ctypes.c_void_p)]
 
 
 class PaOptions(ctypes.Structure):

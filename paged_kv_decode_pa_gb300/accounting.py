@@ -65,3 +65,38 @@ def attention_flops(context_lens, q_heads: int, head_dim: int, num_queries: int 
     for i in range(num_queries):
         pairs += int(np.clip(lens - num_queries + i + 1, 0, None).sum())
     return 4 * head_dim * q_heads * pairs
+
+
+def q8_kv_read_bytes(context_lens, kv_heads: int, head_dim: int, block_size: int = 16) -> int:
+    """int8 pool bytes read for one layer call: one byte per value of K and V for
+    every valid token, its V scale (4 B), and the K scales (4 B per channel) of
+    every block a sequence touches."""
+    lens = np.asarray(context_lens, dtype=np.int64)
+    tokens = int(lens.sum())
+    blocks = int(((lens + block_size - 1) // block_size).sum())
+    return tokens * kv_heads * (2 * head_dim + 4) + blocks * kv_heads * head_dim * 4
+
+
+def decode_bytes_q8(context_lens, q_heads: int, kv_heads: int, head_dim: int, num_queries: int = 1,
+                    block_size: int = 16, fused_write: bool | None = None) -> dict:
+    """Algorithmic bytes of one decode or fused verify call over an int8 pool
+    (queries, new rows and outputs are bf16). The fused write reads the new
+    rows and rewrites, per touched block and KV head, the block's K bytes and
+    scales (its requantisation) and the new V rows with their scales."""
+    if fused_write is None:
+        fused_write = num_queries > 1
+    lens = np.asarray(context_lens, dtype=np.int64)
+    batch = lens.size
+    kv = q8_kv_read_bytes(lens, kv_heads, head_dim, block_size)
+    qo = 2 * batch * num_queries * q_heads * head_dim * 2
+    tables = int(((lens + block_size - 1) // block_size).sum()) * 4 + batch * 4
+    new_writes = 0
+    if fused_write:
+        first = np.maximum(lens - num_queries, 0) // block_size
+        last = np.maximum(lens - 1, 0) // block_size
+        touched = int((last - first + 1)[lens > 0].sum())
+        new_tokens = batch * num_queries
+        new_writes = (touched * kv_heads * (block_size * head_dim + head_dim * 4)
+                      + new_tokens * kv_heads * (2 * head_dim * 2 + head_dim + 4) + new_tokens * 4)
+    total = kv + qo + tables + new_writes
+    return {"kv": kv, "q_out": qo, "tables": tables, "new_writes": new_writes, "total": total}

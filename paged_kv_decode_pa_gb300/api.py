@@ -16,7 +16,7 @@ import torch
 
 from . import _lib as L
 
-_DTYPES = {torch.bfloat16: L.PA_DTYPE_BF16, torch.float32: L.PA_DTYPE_F32}
+_DTYPES = {torch.bfloat16: L.PA_DTYPE_BF16, torch.float32: L.PA_DTYPE_F32, torch.uint8: L.PA_DTYPE_INT8}
 _KERNELS = {"auto": L.PA_KERNEL_AUTO, "mma": L.PA_KERNEL_MMA, "simt": L.PA_KERNEL_SIMT,
             "mma_ldg": L.PA_KERNEL_MMA_LDG}
 
@@ -44,14 +44,35 @@ def _need(cond: bool, msg: str):
         raise ValueError(msg)
 
 
-def make_cache(k_cache: torch.Tensor, v_cache: torch.Tensor) -> L.PaCache:
-    """Describe two head-major pools [kv_heads, num_blocks, block_size, head_dim]."""
+def make_cache(k_cache: torch.Tensor, v_cache: torch.Tensor, k_scale: Optional[torch.Tensor] = None,
+               v_scale: Optional[torch.Tensor] = None) -> L.PaCache:
+    """Describe two head-major pools [kv_heads, num_blocks, block_size, head_dim].
+
+    bf16 or fp32 pools hold values. uint8 pools are the int8 format (bytes
+    value + 128) and need fp32 scales: k_scale [kv_heads, num_blocks, head_dim]
+    and v_scale [kv_heads, num_blocks, block_size].
+    """
     _need(k_cache.shape == v_cache.shape and k_cache.dim() == 4, "caches must be equal 4-D tensors")
-    _need(k_cache.dtype == v_cache.dtype and k_cache.dtype in _DTYPES, "cache dtype must be bf16 or fp32")
+    _need(k_cache.dtype == v_cache.dtype and k_cache.dtype in _DTYPES, "cache dtype must be bf16, fp32 or uint8")
     _need(k_cache.is_cuda and v_cache.is_cuda, "caches must be CUDA tensors")
     _need(k_cache.is_contiguous() and v_cache.is_contiguous(), "caches must be contiguous")
     hkv, nb, bs, d = k_cache.shape
-    return L.PaCache(k_cache.data_ptr(), v_cache.data_ptr(), hkv, nb, bs, d, _DTYPES[k_cache.dtype])
+    dt = _DTYPES[k_cache.dtype]
+    if dt != L.PA_DTYPE_INT8:
+        return L.PaCache(k_cache.data_ptr(), v_cache.data_ptr(), hkv, nb, bs, d, dt, None, None)
+    _need(k_scale is not None and v_scale is not None, "an int8 pool needs k_scale and v_scale")
+    _need(k_scale.dtype == torch.float32 and v_scale.dtype == torch.float32, "scales must be fp32")
+    _need(tuple(k_scale.shape) == (hkv, nb, d) and tuple(v_scale.shape) == (hkv, nb, bs),
+          "k_scale must be [kv_heads, num_blocks, head_dim], v_scale [kv_heads, num_blocks, block_size]")
+    _need(k_scale.is_cuda and v_scale.is_cuda and k_scale.is_contiguous() and v_scale.is_contiguous(),
+          "scales must be contiguous CUDA tensors")
+    return L.PaCache(k_cache.data_ptr(), v_cache.data_ptr(), hkv, nb, bs, d, dt, k_scale.data_ptr(),
+                     v_scale.data_ptr())
+
+
+def _row_dtype(k_cache: torch.Tensor):
+    """dtype of queries, new rows and outputs for this pool (bf16 for int8)."""
+    return torch.bfloat16 if k_cache.dtype == torch.uint8 else k_cache.dtype
 
 
 @functools.lru_cache(maxsize=64)
@@ -92,11 +113,13 @@ def pa_workspace_status(workspace: torch.Tensor, stream=None) -> int:
     return int(flags.value)
 
 
-def pa_cache_write(k_cache, v_cache, k_new, v_new, slot_mapping, stream=None) -> None:
-    cache = make_cache(k_cache, v_cache)
+def pa_cache_write(k_cache, v_cache, k_new, v_new, slot_mapping, stream=None, k_scale=None,
+                   v_scale=None) -> None:
+    cache = make_cache(k_cache, v_cache, k_scale, v_scale)
     n = int(slot_mapping.shape[0])
     _need(slot_mapping.dtype == torch.int32, "slot_mapping must be int32")
-    _need(k_new.dtype == k_cache.dtype and v_new.dtype == k_cache.dtype, "new rows must match the cache dtype")
+    rd = _row_dtype(k_cache)
+    _need(k_new.dtype == rd and v_new.dtype == rd, "new rows must match the cache dtype (bf16 for int8)")
     _need(tuple(k_new.shape) == (n, cache.kv_heads, cache.head_dim) and k_new.shape == v_new.shape,
           "new rows must be [num_tokens, kv_heads, head_dim]")
     _need(k_new.is_contiguous() and v_new.is_contiguous() and slot_mapping.is_contiguous(),
@@ -116,10 +139,11 @@ def _tables(block_tables, context_lens, batch):
 
 def pa_decode(k_cache, v_cache, q, block_tables, context_lens, max_context_len: int, scale: float,
               workspace, out=None, split_tokens: int = 0, kernel: str = "auto", stream=None,
-              prefetch: int = 0, warps: int = 0):
+              prefetch: int = 0, warps: int = 0, k_scale=None, v_scale=None):
     """out[b, hq] = softmax(scale * q[b, hq] . K_b^T) V_b over sequence b's paged context."""
-    cache = make_cache(k_cache, v_cache)
-    _need(q.dim() == 3 and q.dtype == k_cache.dtype and q.is_contiguous(), "q must be [batch, q_heads, head_dim]")
+    cache = make_cache(k_cache, v_cache, k_scale, v_scale)
+    _need(q.dim() == 3 and q.dtype == _row_dtype(k_cache) and q.is_contiguous(),
+          "q must be [batch, q_heads, head_dim] of the row dtype")
     batch, q_heads, _ = q.shape
     mbps = _tables(block_tables, context_lens, batch)
     if out is None:
@@ -133,15 +157,17 @@ def pa_decode(k_cache, v_cache, q, block_tables, context_lens, max_context_len: 
 
 
 def pa_decode_noalloc(k_cache, v_cache, q, block_tables, context_lens, max_context_len: int,
-                      scale: float, out=None, split_tokens: int = 0, kernel: str = "auto", stream=None):
+                      scale: float, out=None, split_tokens: int = 0, kernel: str = "auto", stream=None,
+                      k_scale=None, v_scale=None):
     """pa_decode without a caller workspace, for callers that cannot allocate device memory.
 
     The scratch is a fixed library-owned device array (PA_NOALLOC_SCRATCH_BYTES);
     overlapping calls on the GPU race on it. Only ``out`` may be allocated here,
     and only when it is not passed.
     """
-    cache = make_cache(k_cache, v_cache)
-    _need(q.dim() == 3 and q.dtype == k_cache.dtype and q.is_contiguous(), "q must be [batch, q_heads, head_dim]")
+    cache = make_cache(k_cache, v_cache, k_scale, v_scale)
+    _need(q.dim() == 3 and q.dtype == _row_dtype(k_cache) and q.is_contiguous(),
+          "q must be [batch, q_heads, head_dim] of the row dtype")
     batch, q_heads, _ = q.shape
     mbps = _tables(block_tables, context_lens, batch)
     if out is None:
@@ -155,17 +181,18 @@ def pa_decode_noalloc(k_cache, v_cache, q, block_tables, context_lens, max_conte
 
 def pa_verify(k_cache, v_cache, q, k_new, v_new, slot_mapping, block_tables, context_lens,
               max_context_len: int, scale: float, workspace, out=None, split_tokens: int = 0,
-              kernel: str = "auto", stream=None, prefetch: int = 0, warps: int = 0):
+              kernel: str = "auto", stream=None, prefetch: int = 0, warps: int = 0, k_scale=None,
+              v_scale=None):
     """Fused speculative verify: write the new K/V, attend causally. q: [batch, nq, q_heads, head_dim]."""
-    cache = make_cache(k_cache, v_cache)
-    _need(q.dim() == 4 and q.dtype == k_cache.dtype and q.is_contiguous(),
+    cache = make_cache(k_cache, v_cache, k_scale, v_scale)
+    _need(q.dim() == 4 and q.dtype == _row_dtype(k_cache) and q.is_contiguous(),
           "q must be [batch, num_queries, q_heads, head_dim]")
     batch, nq, q_heads, _ = q.shape
     mbps = _tables(block_tables, context_lens, batch)
     _need(slot_mapping.dtype == torch.int32 and tuple(slot_mapping.shape) == (batch * nq,),
           "slot_mapping must be int32 [batch * num_queries]")
     _need(tuple(k_new.shape) == (batch * nq, cache.kv_heads, cache.head_dim) and k_new.shape == v_new.shape
-          and k_new.dtype == k_cache.dtype and v_new.dtype == k_cache.dtype,
+          and k_new.dtype == q.dtype and v_new.dtype == q.dtype,
           "new rows must be [batch * num_queries, kv_heads, head_dim] of the cache dtype")
     if out is None:
         out = torch.empty_like(q)
@@ -179,9 +206,10 @@ def pa_verify(k_cache, v_cache, q, k_new, v_new, slot_mapping, block_tables, con
 
 
 def pa_validate(k_cache, v_cache, block_tables, context_lens, max_context_len: int,
-                slot_mapping=None, num_queries: int = 1, report=None, stream=None):
+                slot_mapping=None, num_queries: int = 1, report=None, stream=None, k_scale=None,
+                v_scale=None):
     """Device check of tables, lengths and slots; returns the 4-word report tensor (int32 view)."""
-    cache = make_cache(k_cache, v_cache)
+    cache = make_cache(k_cache, v_cache, k_scale, v_scale)
     batch = int(context_lens.shape[0])
     mbps = _tables(block_tables, context_lens, batch)
     if report is None:

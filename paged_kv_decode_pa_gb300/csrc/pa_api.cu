@@ -16,6 +16,13 @@ cudaError_t launch_attn_mma(const CUtensorMap& tk, const CUtensorMap& tv, const 
 cudaError_t launch_attn_simt(const AttnParams& p, bool bf16, dim3 grid, cudaStream_t stream);
 cudaError_t launch_attn_ldg(const AttnParams& p, int prefetch, int warps, cudaStream_t stream);
 cudaError_t launch_merge(const AttnParams& p, cudaStream_t stream);
+struct Q8Maps {
+  CUtensorMap k, v, ks, vs;
+};
+cudaError_t launch_attn_q8(const Q8Maps& maps, const AttnParams& p, dim3 grid, bool after_append,
+                           cudaStream_t stream);
+cudaError_t launch_cache_write_q8(const pa_cache* c, const void* k_new, const void* v_new,
+                                  const int32_t* slots, int32_t n, uint32_t* status, cudaStream_t stream);
 }  // namespace pa
 
 namespace {
@@ -31,11 +38,15 @@ pa_status cuda_fail(cudaError_t e) {
 
 bool aligned16(const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u) == 0; }
 
-size_t elem_size(int32_t dtype) { return dtype == PA_DTYPE_F32 ? 4 : 2; }
+size_t elem_size(int32_t dtype) { return dtype == PA_DTYPE_F32 ? 4 : dtype == PA_DTYPE_INT8 ? 1 : 2; }
 
 pa_status check_cache(const pa_cache* c) {
   if (!c || !c->k || !c->v) return PA_ERR_INVALID_ARG;
-  if (c->dtype != PA_DTYPE_F32 && c->dtype != PA_DTYPE_BF16) return PA_ERR_UNSUPPORTED;
+  if (c->dtype != PA_DTYPE_F32 && c->dtype != PA_DTYPE_BF16 && c->dtype != PA_DTYPE_INT8)
+    return PA_ERR_UNSUPPORTED;
+  if (c->dtype == PA_DTYPE_INT8 &&
+      (!c->k_scale || !c->v_scale || !aligned16(c->k_scale) || !aligned16(c->v_scale)))
+    return PA_ERR_INVALID_ARG;
   if (c->head_dim != kHeadDim || c->block_size != kBlockSize) return PA_ERR_UNSUPPORTED;
   if (c->kv_heads <= 0 || c->num_blocks <= 0) return PA_ERR_INVALID_ARG;
   if (c->kv_heads > 65535) return PA_ERR_UNSUPPORTED;
@@ -108,6 +119,39 @@ bool make_pool_map(CUtensorMap* map, void* pool, int32_t kv_heads, int32_t num_b
   return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, pool, dims, strides, box, estr,
              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// The int8 pool's four views: bytes [kv_heads][num_blocks * 16][128] in
+// 16-row x 128-byte boxes (128-byte swizzle), K scales [kv_heads][num_blocks]
+// [128] and V scales [kv_heads][num_blocks][16] fp32 in one-block boxes.
+// Outside the tensor every view reads zeros.
+bool make_q8_maps(Q8Maps* m, const pa_cache* c) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  const cuuint64_t nb = cuuint64_t(c->num_blocks), hkv = cuuint64_t(c->kv_heads);
+  const cuuint32_t estr[3] = {1, 1, 1};
+  cuuint64_t cdims[3] = {cuuint64_t(kHeadDim), nb * kBlockSize, hkv};
+  cuuint64_t cstr[2] = {cuuint64_t(kHeadDim), nb * kBlockSize * kHeadDim};
+  cuuint32_t cbox[3] = {cuuint32_t(kHeadDim), cuuint32_t(kBlockSize), 1};
+  cuuint64_t kdims[3] = {cuuint64_t(kHeadDim), nb, hkv};
+  cuuint64_t kstr[2] = {cuuint64_t(kHeadDim) * 4, nb * kHeadDim * 4};
+  cuuint32_t kbox[3] = {cuuint32_t(kHeadDim), 1, 1};
+  cuuint64_t vdims[3] = {cuuint64_t(kBlockSize), nb, hkv};
+  cuuint64_t vstr[2] = {cuuint64_t(kBlockSize) * 4, nb * kBlockSize * 4};
+  cuuint32_t vbox[3] = {cuuint32_t(kBlockSize), 1, 1};
+  const auto none = CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE;
+  return enc(&m->k, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, c->k, cdims, cstr, cbox, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             none) == CUDA_SUCCESS &&
+         enc(&m->v, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, c->v, cdims, cstr, cbox, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             none) == CUDA_SUCCESS &&
+         enc(&m->ks, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, c->k_scale, kdims, kstr, kbox, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+             none) == CUDA_SUCCESS &&
+         enc(&m->vs, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, c->v_scale, vdims, vstr, vbox, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+             none) == CUDA_SUCCESS;
 }
 
 // ---------------------------------------------------------------------------
@@ -192,7 +236,9 @@ pa_status attend(const pa_cache* cache, const void* q, void* out, const void* k_
   if (split % kBlockSize || split > kMaxSplitTokens) return PA_ERR_UNSUPPORTED;
   int32_t kernel = opts ? opts->kernel : PA_KERNEL_AUTO;
   if (kernel < PA_KERNEL_AUTO || kernel > PA_KERNEL_MMA_LDG) return PA_ERR_UNSUPPORTED;
-  const bool bf16 = cache->dtype == PA_DTYPE_BF16;
+  const bool int8 = cache->dtype == PA_DTYPE_INT8;
+  if (int8 && kernel != PA_KERNEL_AUTO && kernel != PA_KERNEL_MMA) return PA_ERR_UNSUPPORTED;
+  const bool bf16 = cache->dtype == PA_DTYPE_BF16 || int8;  // int8: q / out / new rows are bf16
   if (kernel == PA_KERNEL_AUTO) kernel = bf16 ? PA_KERNEL_MMA : PA_KERNEL_SIMT;
   const bool use_mma = kernel == PA_KERNEL_MMA || kernel == PA_KERNEL_MMA_LDG;
   if (use_mma && !bf16) return PA_ERR_UNSUPPORTED;
@@ -216,6 +262,8 @@ pa_status attend(const pa_cache* cache, const void* q, void* out, const void* k_
   p.v_cache = cache->v;
   p.k_cache_w = cache->k;
   p.v_cache_w = cache->v;
+  p.k_scale_w = int8 ? cache->k_scale : nullptr;
+  p.v_scale_w = int8 ? cache->v_scale : nullptr;
   p.q = q;
   p.out = out;
   p.k_new = k_new;
@@ -254,7 +302,23 @@ pa_status attend(const pa_cache* cache, const void* q, void* out, const void* k_
   cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
 
   cudaError_t e;
-  if (kernel == PA_KERNEL_MMA_LDG) {
+  if (int8) {
+    // Quantised append first (it requantises whole blocks), then attention
+    // as its programmatic dependent; the merge follows if there are splits.
+    // With one row group per (sequence, KV head) the CTA that holds a new
+    // token's block is its only reader, so it requantises the block itself.
+    // With several, the quantised append runs first and attention follows as
+    // its programmatic dependent.
+    Q8Maps maps;
+    if (!make_q8_maps(&maps, cache)) return cuda_fail(cudaErrorInvalidValue);
+    const bool append_first = fused && p.row_groups > 1;
+    p.fused_write = (fused && !append_first) ? 1 : 0;
+    p.wait_append = append_first ? 1 : 0;
+    e = cudaSuccess;
+    if (append_first) e = launch_cache_write_q8(cache, k_new, v_new, slots, batch * nq, p.status, stream);
+    if (e == cudaSuccess) e = launch_attn_q8(maps, p, grid, append_first, stream);
+    if (e == cudaSuccess && p.max_splits > 1) e = launch_merge(p, stream);
+  } else if (kernel == PA_KERNEL_MMA_LDG) {
     e = launch_attn_ldg(p, prefetch, warps, stream);
   } else if (kernel == PA_KERNEL_MMA) {
     CUtensorMap tk, tv;
@@ -294,6 +358,11 @@ pa_status pa_cache_write(const pa_cache* cache, const void* k_new, const void* v
   if (num_tokens == 0) return PA_OK;
   if (!k_new || !v_new || !slot_mapping || !aligned16(k_new) || !aligned16(v_new))
     return PA_ERR_INVALID_ARG;
+  if (cache->dtype == PA_DTYPE_INT8) {
+    const cudaError_t e = launch_cache_write_q8(cache, k_new, v_new, slot_mapping, num_tokens, nullptr,
+                                                static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? PA_OK : cuda_fail(e);
+  }
   const int32_t cpr = int32_t(kHeadDim * elem_size(cache->dtype) / 16);
   const int64_t total = int64_t(num_tokens) * cache->kv_heads * 2 * cpr;
   const int threads = 256;

@@ -29,6 +29,8 @@ struct AttnParams {
   const void* v_cache;
   void* k_cache_w;  // same pools, written by the fused verify
   void* v_cache_w;
+  void* k_scale_w;  // int8 pool: K scales [kv_heads, num_blocks, 128] (fused write)
+  void* v_scale_w;  // int8 pool: V scales [kv_heads, num_blocks, 16]
   const void* q;  // [batch, num_queries, q_heads, 128]
   void* out;      // same shape
   const void* k_new;  // [batch * num_queries, kv_heads, 128] (fused verify only)
@@ -46,6 +48,7 @@ struct AttnParams {
   int32_t row_groups;  // ceil(rows / rows_per_cta)
   int32_t max_context_len, split_tokens, max_splits;
   int32_t fused_write;  // 1: new rows come from k_new/v_new and are written to the cache
+  int32_t wait_append;  // int8: 1 if a preceding append grid wrote the new tokens' blocks
   int32_t merge_in_kernel;  // 1: the last split to finish merges; 0: merge_kernel does
   float scale_log2;     // scale * log2(e): scores are kept in base-2 units
 };
@@ -105,6 +108,10 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
 
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void prefetch_l2(const void* ptr) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(ptr));
 }
 
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {

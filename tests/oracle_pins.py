@@ -298,7 +298,7 @@ def _q8_row(d=128):
     """One row with hand-checked codes at scale 15.875 / 127 = 1/8 (exact)."""
     v = np.zeros(d, np.float32)
     v[:8] = [15.875, -15.875, 0.0, 7.9375, 7.8125, -7.8125, 0.0625, 0.1875]
-    # x / (1/8) = 127, -127, 0, 63.5, 62.5, -62.5, 0.5, 1.5 -> ties go to even.
+    # x * (127 / 15.875 = 8) = 127, -127, 0, 63.5, 62.5, -62.5, 0.5, 1.5 -> ties go to even.
     want = np.full(d, 128, np.uint8)
     want[:8] = [255, 1, 128, 192, 190, 66, 128, 130]
     return v, want
@@ -306,7 +306,8 @@ def _q8_row(d=128):
 
 def pin_q8_row_closed_form(orc):
     """One token into an empty block: V gets the row's own scale and the codes
-    worked out by hand (round to nearest, ties to even, +128 offset); each K
+    worked out by hand (x * 127 / max rounded to nearest, ties to even, +128
+    offset); each K
     channel's scale is |k| / 127 (the row is the only non-zero one), its code
     +-127, and every other row stays byte 128."""
     kq, vq, ks, vs = _empty_q8(1, 2)
@@ -338,8 +339,8 @@ def pin_q8_requant_closed_form(orc):
     assert ks[0, 0, 0] == 0.125 and kq[0, 0, 0, 0] == 255
     orc.cache_write_q8(kq, vq, ks, vs, _bf16(b)[None, None], _bf16(b)[None, None], np.array([1], np.int32))
     assert ks[0, 0, 0] == 0.25 and ks[0, 0, 1] == 0.125
-    assert kq[0, 0, 0, 0] == 192  # 15.875 / 0.25 = 63.5 -> 64
-    assert kq[0, 0, 1, 0] == 255 and kq[0, 0, 0, 1] == 255 and kq[0, 0, 1, 1] == 136  # 1 / 0.125 = 8
+    assert kq[0, 0, 0, 0] == 192  # 15.875 * (127 / 31.75 = 4) = 63.5 -> 64
+    assert kq[0, 0, 1, 0] == 255 and kq[0, 0, 0, 1] == 255 and kq[0, 0, 1, 1] == 136  # 1 * 8 = 8
     # V rows are independent: the first row's V is untouched by the second write.
     assert vs[0, 0, 0] == 0.125 and vs[0, 0, 1] == 0.25 and vq[0, 0, 0, 0] == 255
 

@@ -113,3 +113,18 @@ def test_workspace_size(lib):
 def test_status_strings(lib):
     assert lib.pa_status_string(_lib.PA_ERR_WORKSPACE) == b"PA_ERR_WORKSPACE"
     assert lib.pa_version() >= 100
+
+
+def test_int8_pool_arguments(lib):
+    """An int8 pool needs 16-byte aligned scale arrays and runs only on the
+    tensor-core kernel; the dtype value matches the header."""
+    text = HEADER.read_text()
+    assert re.search(r"PA_DTYPE_INT8 = (\d+)", text).group(1) == str(_lib.PA_DTYPE_INT8)
+    ok = dict(dtype=_lib.PA_DTYPE_INT8, k_scale=0x110000, v_scale=0x120000)
+    assert _decode(lib, _cache(**ok), batch=0) == _lib.PA_OK
+    assert _decode(lib, _cache(**{**ok, "k_scale": None})) == _lib.PA_ERR_INVALID_ARG
+    assert _decode(lib, _cache(**{**ok, "v_scale": 0x120004})) == _lib.PA_ERR_INVALID_ARG
+    for kernel in (_lib.PA_KERNEL_SIMT, _lib.PA_KERNEL_MMA_LDG):
+        assert _decode(lib, _cache(**ok), opts=_lib.PaOptions(0, kernel)) == _lib.PA_ERR_UNSUPPORTED
+    assert lib.pa_cache_write(ctypes.byref(_cache(**{**ok, "k_scale": None})), 0x80000, 0x90000, 0xa0000, 4,
+                              None) == _lib.PA_ERR_INVALID_ARG

@@ -38,3 +38,18 @@ def test_flops_count_visible_pairs_only():
     assert accounting.attention_flops(lens, q_heads=2, head_dim=4) == 4 * 4 * 2 * 8
     # verify with two queries: rows see L-1 and L tokens
     assert accounting.attention_flops(lens, q_heads=1, head_dim=1, num_queries=2) == 4 * (2 + 4 + 3 + 5)
+
+
+def test_q8_bytes_per_block():
+    """One full 16-token block of one KV head in the int8 pool: 2 x 2048 code
+    bytes, 16 V scales and 128 K scales of 4 bytes = 4,672 bytes (against 8,192
+    in bf16)."""
+    from paged_kv_decode_pa_gb300 import accounting
+
+    assert accounting.q8_kv_read_bytes([16], 1, 128) == 4672
+    assert accounting.kv_read_bytes([16], 1, 128, 2) == 8192
+    # a partial block still carries the block's K scales
+    assert accounting.q8_kv_read_bytes([1], 1, 128) == 2 * 128 + 4 + 512
+    b = accounting.decode_bytes_q8([17, 0], q_heads=2, kv_heads=1, head_dim=128, num_queries=2)
+    # new tokens at positions 15, 16: two touched blocks for the first sequence, none for L = 0
+    assert b["new_writes"] == 2 * (16 * 128 + 128 * 4) + 4 * (2 * 128 * 2 + 128 + 4) + 4 * 4

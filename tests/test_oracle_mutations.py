@@ -44,8 +44,9 @@ MUTATIONS = {
                                 "uint32_t bits = ((uint32_t)((const uint16_t *)base)[index]) << 15;"),
     # int8 pool
     "q8_offset_127": ("return (uint8_t)((int)r + 128);", "return (uint8_t)((int)r + 127);"),
-    "q8_floor_not_nearest": ("float r = rintf(x / s);", "float r = floorf(x / s);"),
-    "q8_ties_away_from_zero": ("float r = rintf(x / s);", "float r = roundf(x / s);"),
+    "q8_floor_not_nearest": ("float r = rintf(x * inv);", "float r = floorf(x * inv);"),
+    "q8_ties_away_from_zero": ("float r = rintf(x * inv);", "float r = roundf(x * inv);"),
+    "q8_inverse_of_128": ("return maxabs == 0.0f ? 0.0f : 127.0f / maxabs; }", "return maxabs == 0.0f ? 0.0f : 128.0f / maxabs; }"),
     "q8_scale_over_128": ("return maxabs / 127.0f; }", "return maxabs / 128.0f; }"),
     "q8_dequant_without_offset": ("return (float)((int)byte - 128) * s; }", "return (float)((int)byte) * s; }"),
     "q8_k_scale_kept": ("ks[d] = q8_scale(m);", "(void)m;"),
@@ -56,7 +57,8 @@ MUTATIONS = {
                         "const uint16_t *src = k_new + ((int64_t)j * kv_heads + h) * head_dim;"),
     "q8_k_scale_per_row": ("for (int r = 0; r < block_size; ++r) {\n                    const float a = fabsf(x[r * head_dim + d]);",
                            "for (int r = 0; r < 1; ++r) {\n                    const float a = fabsf(x[r * head_dim + d]);"),
-    "q8_v_scale_of_wrong_row": ("v_scale[blk * block_size + r] = s;", "v_scale[blk * block_size + (r + 1) % block_size] = s;"),
+    "q8_v_scale_of_wrong_row": ("v_scale[blk * block_size + r] = q8_scale(m);",
+                                "v_scale[blk * block_size + (r + 1) % block_size] = q8_scale(m);"),
 }
 
 

@@ -53,6 +53,8 @@ def parse_args():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--workload", default="c4", choices=["c2", "c3", "c4", "c5"])
+    ap.add_argument("--kv", default="bf16", choices=["bf16", "int8"],
+                    help="KV pool format (int8: bytes + scales, dequantised inside the kernel)")
     ap.add_argument("--no-extra", action="store_true", help="skip the per_config measurements")
     ap.add_argument("--kernel", default="auto", choices=["auto", "mma", "mma_ldg", "simt"])
     ap.add_argument("--prefetch", type=int, default=0, help="blocks in flight per warp (mma_ldg kernel)")
@@ -430,6 +432,32 @@ def step_bytes(w, fused=True, kv="bf16"):
     return att, write
 
 
+def launches_per_step(w, step, split: int, kernel: str, kv: str) -> int:
+    """libpa kernels one step launches: the append when it is not fused, the
+    attention kernel, the log-sum-exp merge when a call has several splits
+    (tensor-core paths), and, for an int8 pool whose (sequence, KV head) rows
+    span several row groups, the quantised append ahead of a fused verify."""
+    from paged_kv_decode_pa_gb300 import _lib
+
+    s = w.spec
+    max_ctx = w.max_context_len
+    if split:
+        size = split
+    elif max_ctx > _lib.PA_LONG_CONTEXT_TOKENS:
+        size = _lib.PA_DEFAULT_SPLIT_LONG_INT8 if kv == "int8" else _lib.PA_DEFAULT_SPLIT_LONG
+    else:
+        size = _lib.PA_DEFAULT_SPLIT_TOKENS
+    splits = max(1, -(-max_ctx // size))
+    n = (0 if step.fused else 1) + 1
+    tensor_core = kv == "int8" or (kernel in ("auto", "mma", "mma_ldg") and s.dtype == "bf16")
+    if tensor_core and splits > 1:
+        n += 1
+    rows = s.num_queries * (s.q_heads // s.kv_heads)
+    if kv == "int8" and step.fused and rows > 16:
+        n += 1
+    return n
+
+
 def measure_extra(name, device, steps, flush, split, kernel, prefetch=0, warps=0, fused=True, graph=False,
                   kv="bf16"):
     w = inputs.make(name)
@@ -470,10 +498,10 @@ def run_native(args):
     _lib.load()  # fails loudly if the library is missing
     w = rank_workload(args.workload, rank)
     step = DecodeStep(w, device, args.split_tokens, args.kernel, args.prefetch, args.warps,
-                      fused=not args.unfused)
+                      fused=not args.unfused, kv=args.kv)
     flush = make_l2_flush(device)
 
-    att, write = step_bytes(w, step.fused)
+    att, write = step_bytes(w, step.fused, args.kv)
     barrier(world)
     torch.cuda.synchronize()
     with ClockSampler(local) as clocks:
@@ -494,7 +522,7 @@ def run_native(args):
     value = whole_job_gbs(att["kv"], world, ms_step)
     peak, peak_kind = hbm_peak()
     achieved = att["total"] / (ms_attend * 1e-3) / 1e9
-    traffic = ncu_traffic(args.workload)
+    traffic = ncu_traffic(args.workload if args.kv == "bf16" else f"{args.workload}_{args.kv}")
 
     extra = {}
     if not args.no_extra and rank == 0:
@@ -508,7 +536,7 @@ def run_native(args):
             extra[name + "_int8"] = measure_extra(name, device, 20, flush, args.split_tokens, "auto", 0, 0,
                                                   not args.unfused, args.graph, kv="int8")
 
-    cpu = cpu_baseline(w, args.cpu_seconds) if rank == 0 else None
+    cpu = cpu_baseline(w, args.cpu_seconds, args.kv) if rank == 0 else None
 
     if rank == 0:
         s = w.spec
@@ -527,15 +555,19 @@ def run_native(args):
             "higher_is_better": True,
             "scaling": "weak",
             "vs_baseline": None,
-            "dtype": s.dtype,
+            "dtype": s.dtype if args.kv == "bf16" else "int8 pool, bf16 queries",
             "data": "synthetic (seeded N(0,1) bf16; no dataset or weights involved)",
             "config": {
                 "workload": f"{args.workload}: {s.description}",
                 "batch": s.batch, "q_heads": s.q_heads, "kv_heads": s.kv_heads, "head_dim": s.head_dim,
                 "block_size": s.block_size, "num_blocks": s.num_blocks,
                 "context_tokens": int(w.context_lens.sum()),
-                "split_tokens": args.split_tokens or _lib.PA_DEFAULT_SPLIT_TOKENS,
+                "split_tokens": args.split_tokens or (
+                    f"default: {_lib.PA_DEFAULT_SPLIT_TOKENS} up to {_lib.PA_LONG_CONTEXT_TOKENS} tokens, "
+                    f"{_lib.PA_DEFAULT_SPLIT_LONG_INT8 if args.kv == 'int8' else _lib.PA_DEFAULT_SPLIT_LONG} "
+                    f"beyond"),
                 "kernel": args.kernel,
+                "kv": args.kv,
                 "launch": "CUDA graph replay of the step" if args.graph else "direct launches",
                 **({"prefetch": args.prefetch or 1, "warps_per_split": args.warps or 4}
                    if args.kernel == "mma_ldg" else {}),
@@ -549,9 +581,10 @@ def run_native(args):
             },
             "roofline": {
                 "bound": "hbm",
-                "kernel": {"auto": "pa_decode (attn_mma_kernel)", "mma": "pa_decode (attn_mma_kernel)",
-                           "mma_ldg": "pa_decode (attn_ldg_kernel)",
-                           "simt": "pa_decode (attn_simt_kernel)"}[args.kernel],
+                "kernel": ("pa_decode (attn_q8_kernel)" if args.kv == "int8" else
+                           {"auto": "pa_decode (attn_mma_kernel)", "mma": "pa_decode (attn_mma_kernel)",
+                            "mma_ldg": "pa_decode (attn_ldg_kernel)",
+                            "simt": "pa_decode (attn_simt_kernel)"}[args.kernel]),
                 "achieved": round(achieved, 1),
                 "peak": peak,
                 "unit": "GB/s",
@@ -566,10 +599,7 @@ def run_native(args):
                     "ms_per_step": round(e2e_step, 5), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                     "path": "one pinned host -> device copy of the step's inputs (StepStaging), the step's libpa call(s), "
                             "device -> host copy of the output"},
-            "gpu_launches": ((0 if step.fused else 1) + 1
-                             + (1 if args.kernel == "mma_ldg" and w.max_context_len > (args.split_tokens or
-                                                                                    _lib.PA_DEFAULT_SPLIT_TOKENS) else 0))
-                            * args.steps,
+            "gpu_launches": launches_per_step(w, step, args.split_tokens, args.kernel, args.kv) * args.steps,
             "clocks": clocks.summary(),
             "wall_s_timed_loop": round(wall, 3),
             "per_config": extra,
@@ -584,25 +614,33 @@ def run_native(args):
 # ---------------------------------------------------------------------------
 # CPU baseline: the fp64 oracle, as it stands, on a bounded sample
 
-def cpu_baseline(w, budget_s: float):
+def cpu_baseline(w, budget_s: float, kv_format: str = "bf16"):
     import oracle
 
     cores = os.cpu_count() or 1
     oracle.set_threads(cores)
     s = w.spec
-    kc, vc = w.k_cache, w.v_cache
-    q = w.q if s.num_queries > 1 else w.q
+    if kv_format == "int8":
+        # The oracle's int8 attention: dequantise the pool (fp32), then the fp64 attention.
+        pool = inputs.q8_pool(w)
+        kc, vc = oracle.dequant_q8(pool.k_codes, pool.v_codes, pool.k_scale, pool.v_scale)
+        q = oracle.bf16_bits_to_f64(w.q).astype(np.float32)
+    else:
+        kc, vc = w.k_cache, w.v_cache
+        q = w.q
     done, elapsed = 0, 0.0
     chunk = max(1, min(s.batch, cores))
     used_threads = min(cores, chunk)
     while done < s.batch and elapsed < budget_s:
         b1 = min(s.batch, done + chunk)
         t0 = time.perf_counter()
-        oracle.attend(kc, vc, q if q.ndim == 4 else q, w.block_tables, w.context_lens, w.scale, (done, b1))
+        oracle.attend(kc, vc, q, w.block_tables, w.context_lens, w.scale, (done, b1))
         elapsed += time.perf_counter() - t0
         done = b1
-    eb = accounting.elem_bytes(s.dtype)
-    kv = accounting.kv_read_bytes(w.context_lens[:done], s.kv_heads, s.head_dim, eb)
+    if kv_format == "int8":
+        kv = accounting.q8_kv_read_bytes(w.context_lens[:done], s.kv_heads, s.head_dim)
+    else:
+        kv = accounting.kv_read_bytes(w.context_lens[:done], s.kv_heads, s.head_dim, accounting.elem_bytes(s.dtype))
     return {"value": round(kv / elapsed / 1e9, 3), "unit": "GB/s", "cores": used_threads,
             "kind": "oracle",
             "sample": f"{done} of {s.batch} sequences ({int(w.context_lens[:done].sum())} tokens), "

@@ -130,10 +130,13 @@ typedef enum pa_kernel {
 
 /* Optional tuning for pa_decode / pa_verify; pass NULL for the defaults. */
 typedef struct pa_options {
-    /* Tokens per context split (flash-decoding split-K). 0 = default
-     * (PA_DEFAULT_SPLIT_TOKENS). Must be a positive multiple of block_size.
-     * A sequence's result depends only on its own length and this value, never
-     * on its batch-mates, so it is bit-identical across batch compositions. */
+    /* Tokens per context split (flash-decoding split-K). A positive multiple
+     * of block_size: every sequence uses this split. 0 = the default rule:
+     * PA_DEFAULT_SPLIT_TOKENS for a sequence of up to PA_LONG_CONTEXT_TOKENS
+     * tokens, and PA_DEFAULT_SPLIT_LONG (bf16, fp32) or
+     * PA_DEFAULT_SPLIT_LONG_INT8 (int8 pool) for a longer one. Either way a
+     * sequence's split depends only on its own length, never on its
+     * batch-mates, so its result is bit-identical across batch compositions. */
     int32_t split_tokens;
     int32_t kernel;   /* pa_kernel */
     /* PA_KERNEL_MMA_LDG only: 16-token blocks each warp keeps in flight, 1 or 2;
@@ -149,6 +152,9 @@ typedef struct pa_options {
 #define PA_DEFAULT_WARPS 4
 
 #define PA_DEFAULT_SPLIT_TOKENS 1536
+#define PA_LONG_CONTEXT_TOKENS 4096
+#define PA_DEFAULT_SPLIT_LONG 1024
+#define PA_DEFAULT_SPLIT_LONG_INT8 768
 
 /*
  * pa_cache_write: cache[h, s / 16, s % 16, :] = new[i, h, :] for every token

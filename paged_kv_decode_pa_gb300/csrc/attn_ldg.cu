@@ -81,12 +81,13 @@ __global__ void __launch_bounds__(32 * W, ((NT == 1 && PF == 1) ? 12 : 8) / W)
     if (threadIdx.x == 0 && split == 0 && h == 0 && rg == 0) raise_flag(p.status, PA_FLAG_BAD_LENGTH);
     L = L < 0 ? 0 : cap;
   }
-  const int nsplit = (L + p.split_tokens - 1) / p.split_tokens;
+  const int ssize = split_for(p, L);
+  const int nsplit = (L + ssize - 1) / ssize;
   if (split >= max(nsplit, 1)) return;  // uniform across the CTA
   const int row0 = rg * p.rows_per_cta;
   const int nrows = min(p.rows_per_cta, p.rows - row0);
-  const int t0 = split * p.split_tokens;
-  const int t1 = min(L, t0 + p.split_tokens);
+  const int t0 = split * ssize;
+  const int t1 = min(L, t0 + ssize);
   const int nblk = (t1 - t0 + kBlockSize - 1) / kBlockSize;
   const int new0 = L - p.num_queries;  // first position of a new (verify) token
   const bool fused = p.fused_write != 0;

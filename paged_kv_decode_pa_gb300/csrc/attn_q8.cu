@@ -199,6 +199,15 @@ __global__ void __launch_bounds__(kQ8Threads, NT == 1 ? 5 : 3)
       s_ids[j] = __ldg(p.block_tables + int64_t(b) * p.mbps + j0 + j);
   }
   const CtaWork w = cta_work(p, L_raw);
+  if (w.split_size != p.split_tokens) {
+    // A long sequence with its own split size: its entries start elsewhere.
+    // Each thread rewrites the indices it wrote above, so no barrier is needed.
+    const int b = blockIdx.z / p.row_groups;
+    const int j0 = w.t0 / kBlockSize;
+    const int jn = min(w.split_size / kBlockSize, p.mbps - j0);
+    for (int j = threadIdx.x; j < jn; j += blockDim.x)
+      s_ids[j] = __ldg(p.block_tables + int64_t(b) * p.mbps + j0 + j);
+  }
   if (w.split >= w.nsplit) {
     if (w.L == 0 && w.split == 0) write_zero_rows<uint16_t>(p, w);
     return;

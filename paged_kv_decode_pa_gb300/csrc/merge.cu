@@ -40,7 +40,8 @@ __global__ void __launch_bounds__(kMergeWarps * 32) merge_kernel(const AttnParam
   const int cap = min(p.max_context_len, p.mbps * kBlockSize);
   int L = __ldg(p.context_lens + b);
   L = L < 0 ? 0 : min(L, cap);
-  const int nsplit = (L + p.split_tokens - 1) / p.split_tokens;
+  const int split = split_for(p, L);
+  const int nsplit = (L + split - 1) / split;
   if (nsplit <= 1) return;  // written by the attention kernel itself
 
   pdl_wait_primary();

@@ -60,6 +60,22 @@ int32_t split_of(const pa_options* o) {
   return (o && o->split_tokens > 0) ? o->split_tokens : PA_DEFAULT_SPLIT_TOKENS;
 }
 
+// Split for sequences longer than PA_LONG_CONTEXT_TOKENS under the default
+// rule (0: an explicit split applies to every length). Without a dtype
+// (workspace sizing) the finer of the two is taken, an upper bound on splits.
+int32_t split_long_of(const pa_options* o, int32_t dtype) {
+  if (o && o->split_tokens > 0) return 0;
+  if (dtype == PA_DTYPE_INT8 || dtype < 0) return PA_DEFAULT_SPLIT_LONG_INT8;
+  return PA_DEFAULT_SPLIT_LONG;
+}
+
+// Most splits any sequence of up to max_ctx tokens can have: the split
+// count grows with the length under either rule.
+int64_t max_splits_of(int32_t max_ctx, int32_t split, int32_t split_long) {
+  const int32_t s = (split_long > 0 && max_ctx > PA_LONG_CONTEXT_TOKENS) ? split_long : split;
+  return std::max<int64_t>(1, (int64_t(max_ctx) + s - 1) / s);
+}
+
 // Workspace: [status word | counters | lse partials | o partials], each
 // region 256-byte aligned. Row groups are counted for the 8-row CUDA-core
 // kernel, an upper bound for the 16-row tensor-core kernel.
@@ -72,12 +88,12 @@ struct WsLayout {
 size_t round256(size_t x) { return (x + 255) & ~size_t(255); }
 
 bool ws_layout(int32_t batch, int32_t nq, int32_t q_heads, int32_t kv_heads, int32_t max_ctx,
-               int32_t split, WsLayout* out) {
+               int32_t split, int32_t split_long, WsLayout* out) {
   if (batch < 0 || nq < 1 || q_heads <= 0 || kv_heads <= 0 || q_heads % kv_heads) return false;
   if (max_ctx < 0 || split <= 0) return false;
   const int64_t rows = int64_t(nq) * (q_heads / kv_heads);
   const int64_t groups = (rows + 7) / 8;
-  const int64_t splits = std::max<int64_t>(1, (int64_t(max_ctx) + split - 1) / split);
+  const int64_t splits = max_splits_of(max_ctx, split, split_long);
   const int64_t units = int64_t(batch) * kv_heads * groups;
   WsLayout L;
   L.max_splits = static_cast<int32_t>(splits);
@@ -253,7 +269,8 @@ pa_status attend(const pa_cache* cache, const void* q, void* out, const void* k_
   if (fused && (!v_new || !slots || !aligned16(k_new) || !aligned16(v_new))) return PA_ERR_INVALID_ARG;
 
   WsLayout L;
-  if (!ws_layout(batch, nq, q_heads, cache->kv_heads, max_ctx, split, &L)) return PA_ERR_INVALID_ARG;
+  const int32_t split_long = split_long_of(opts, cache->dtype);
+  if (!ws_layout(batch, nq, q_heads, cache->kv_heads, max_ctx, split, split_long, &L)) return PA_ERR_INVALID_ARG;
   if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u) || ws_bytes < L.total) return PA_ERR_WORKSPACE;
 
   AttnParams p;
@@ -288,6 +305,8 @@ pa_status attend(const pa_cache* cache, const void* q, void* out, const void* k_
   p.row_groups = (p.rows + p.rows_per_cta - 1) / p.rows_per_cta;
   p.max_context_len = max_ctx;
   p.split_tokens = split;
+  p.split_long = split_long;
+  p.long_from = PA_LONG_CONTEXT_TOKENS;
   p.max_splits = L.max_splits;
   p.fused_write = fused ? 1 : 0;
   // The CUDA-core kernel merges in its last split; the tensor-core kernels
@@ -342,7 +361,7 @@ namespace pa {
 size_t workspace_zero_prefix(int32_t batch, int32_t nq, int32_t q_heads, int32_t kv_heads,
                              int32_t max_ctx, int32_t split) {
   WsLayout L;
-  return ws_layout(batch, nq, q_heads, kv_heads, max_ctx, split, &L) ? L.lse : 0;
+  return ws_layout(batch, nq, q_heads, kv_heads, max_ctx, split, split_long_of(nullptr, -1), &L) ? L.lse : 0;
 }
 
 void record_cuda_error(cudaError_t e) { g_last_cuda_error = static_cast<int>(e); }
@@ -379,7 +398,9 @@ size_t pa_workspace_size(int32_t batch, int32_t num_queries, int32_t q_heads, in
                          int32_t head_dim, int32_t max_context_len, const pa_options* opts) {
   if (head_dim != kHeadDim) return 0;
   WsLayout L;
-  if (!ws_layout(batch, num_queries, q_heads, kv_heads, max_context_len, split_of(opts), &L)) return 0;
+  if (!ws_layout(batch, num_queries, q_heads, kv_heads, max_context_len, split_of(opts),
+                 split_long_of(opts, -1), &L))
+    return 0;
   return L.total;
 }
 

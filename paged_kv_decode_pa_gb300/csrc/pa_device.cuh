@@ -47,6 +47,8 @@ struct AttnParams {
   int32_t rows_per_cta;  // 16 (tensor-core kernel) or 8 (CUDA-core kernel)
   int32_t row_groups;  // ceil(rows / rows_per_cta)
   int32_t max_context_len, split_tokens, max_splits;
+  int32_t split_long;   // > 0: sequences longer than long_from tokens use this split instead
+  int32_t long_from;
   int32_t fused_write;  // 1: new rows come from k_new/v_new and are written to the cache
   int32_t wait_append;  // int8: 1 if a preceding append grid wrote the new tokens' blocks
   int32_t merge_in_kernel;  // 1: the last split to finish merges; 0: merge_kernel does
@@ -199,9 +201,15 @@ __device__ __forceinline__ void raise_flag(uint32_t* status, uint32_t bits) {
 // ---------------------------------------------------------------------------
 // Per-CTA work description
 
+// Tokens per split for a sequence of length L (depends on L alone).
+__device__ __forceinline__ int split_for(const AttnParams& p, int L) {
+  return (p.split_long > 0 && L > p.long_from) ? p.split_long : p.split_tokens;
+}
+
 struct CtaWork {
   int b, h, rg, split;
   int L;          // clamped context length
+  int split_size; // tokens per split of this sequence
   int nsplit;     // non-empty splits of this sequence
   int t0, t1;     // token range of this split
   int row0;       // first row of this row group
@@ -224,9 +232,10 @@ __device__ __forceinline__ CtaWork cta_work(const AttnParams& p, int L_raw = -21
     L = L < 0 ? 0 : cap;
   }
   w.L = L;
-  w.nsplit = (L + p.split_tokens - 1) / p.split_tokens;
-  w.t0 = w.split * p.split_tokens;
-  w.t1 = min(L, w.t0 + p.split_tokens);
+  w.split_size = split_for(p, L);
+  w.nsplit = (L + w.split_size - 1) / w.split_size;
+  w.t0 = w.split * w.split_size;
+  w.t1 = min(L, w.t0 + w.split_size);
   w.row0 = w.rg * p.rows_per_cta;
   w.nrows = min(p.rows_per_cta, p.rows - w.row0);
   w.unit = (w.b * p.kv_heads + w.h) * p.row_groups + w.rg;

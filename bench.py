@@ -60,6 +60,9 @@ def parse_args():
     ap.add_argument("--prefetch", type=int, default=0, help="blocks in flight per warp (mma_ldg kernel)")
     ap.add_argument("--warps", type=int, default=0, help="warps per split (mma_ldg kernel)")
     ap.add_argument("--split-tokens", type=int, default=0)
+    ap.add_argument("--buckets", action="store_true",
+                    help="also time the Qwen2-shaped decode step per batch bucket (1..64), direct and as "
+                         "CUDA-graph replays")
     ap.add_argument("--graph", action="store_true",
                     help="time each step as a replay of a captured CUDA graph of the step")
     ap.add_argument("--unfused", action="store_true",
@@ -432,6 +435,25 @@ def step_bytes(w, fused=True, kv="bf16"):
     return att, write
 
 
+def measure_graph_buckets(device, flush, steps: int = 20) -> dict:
+    """The engine pattern of one CUDA graph per batch bucket ("From 183 ms to
+    19 ms per decode step", section "4. CUDA graphs per batch bucket"): for
+    each bucket a Qwen2-1.5B-shaped decode step (pa_cache_write of one token per
+    sequence, then pa_decode) over fixed buffers, timed as direct launches and
+    as a replay of its captured graph."""
+    out = {}
+    for batch in (1, 2, 4, 8, 16, 32, 64):
+        w = inputs.make("c2", batch=batch, num_blocks=max(4096, batch * 40))
+        st = DecodeStep(w, device, fused=False)
+        direct, _ = time_steps(st, steps, 3, flush)
+        replay, _ = time_steps(st, steps, 3, flush, graph=True)
+        out[str(batch)] = {"direct_us": round(statistics.mean(direct) * 1e3, 2),
+                           "graph_replay_us": round(statistics.mean(replay) * 1e3, 2),
+                           "kv_mb": round(step_bytes(w, False)[0]["kv"] / 1e6, 2)}
+        del st
+    return out
+
+
 def launches_per_step(w, step, split: int, kernel: str, kv: str) -> int:
     """libpa kernels one step launches: the append when it is not fused, the
     attention kernel, the log-sum-exp merge when a call has several splits
@@ -530,6 +552,8 @@ def run_native(args):
             if name != args.workload:
                 extra[name] = measure_extra(name, device, 20, flush, args.split_tokens, args.kernel,
                                             args.prefetch, args.warps, not args.unfused, args.graph)
+        if args.buckets:
+            extra["graph_buckets_c2"] = measure_graph_buckets(device, flush)
         # The int8 pool (the next row of the scope): the same workloads with
         # dequantisation fused into the attention kernel.
         for name in ("c4", "c3", "c5"):

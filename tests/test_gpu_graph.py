@@ -72,3 +72,45 @@ def test_graph_replay_tracks_inputs(name, split):
         got = pa.to_numpy(out)
         assert_close(to_f64(got), ref, "bf16", f"{name} graph replay {trial}")
         assert np.array_equal(pa.to_numpy(kc), kc0) and np.array_equal(pa.to_numpy(vc), vc0)
+
+
+@pytest.mark.parametrize("batch", [1, 8, 64])
+def test_bucket_graph_write_then_decode(batch):
+    """One graph per batch bucket: pa_cache_write + pa_decode captured over fixed
+    buffers and replayed; the replay matches the oracle's write-then-decode."""
+    import torch
+
+    import paged_kv_decode_pa_gb300 as pa
+
+    w = inputs.make("c2", batch=batch, num_blocks=max(4096, batch * 40))
+    dev = torch.device("cuda")
+    kc, vc = pa.to_torch(w.k_cache, dev), pa.to_torch(w.v_cache, dev)
+    q, kn, vn = pa.to_torch(w.q, dev), pa.to_torch(w.k_new, dev), pa.to_torch(w.v_new, dev)
+    slots, tables, lens = (pa.to_torch(w.slot_mapping, dev), pa.to_torch(w.block_tables, dev),
+                           pa.to_torch(w.context_lens, dev))
+    ws = pa.new_workspace(batch, 1, w.spec.q_heads, w.spec.kv_heads, w.max_context_len, dev)
+    out = torch.empty_like(q)
+
+    def step():
+        pa.pa_cache_write(kc, vc, kn, vn, slots)
+        pa.pa_decode(kc, vc, q, tables, lens, w.max_context_len, w.scale, ws, out=out)
+
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        step()
+    torch.cuda.current_stream().wait_stream(side)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        step()
+    kc.copy_(pa.to_torch(w.k_cache, dev))
+    vc.copy_(pa.to_torch(w.v_cache, dev))
+    out.zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    assert pa.pa_workspace_status(ws) == 0
+    rk, rv = w.k_cache.copy(), w.v_cache.copy()
+    assert oracle.cache_write(rk, rv, w.k_new, w.v_new, w.slot_mapping) == 0
+    ref = oracle.decode(rk, rv, w.q, w.block_tables, w.context_lens, w.scale)
+    assert_close(to_f64(pa.to_numpy(out)), ref, "bf16", f"bucket {batch}")
+    assert np.array_equal(pa.to_numpy(kc), rk) and np.array_equal(pa.to_numpy(vc), rv)

@@ -264,6 +264,36 @@ pa_status pa_verify(const pa_cache *cache, const void *d_q, void *d_out, const v
                     size_t workspace_bytes, const pa_options *opts, void *stream);
 
 /*
+ * pa_verify_ragged: pa_verify for sequences with different numbers of new
+ * tokens in one launch: decode sequences (one token) and verify sequences
+ * (k+1 tokens) side by side, none padded ("From 183 ms to 19 ms per decode
+ * step", section "Then speculative decoding got slower": padded guesses cost
+ * a second set of graphs). Sequence b has n_b = query_start[b+1] -
+ * query_start[b] new tokens, at positions L - n_b + i (L = context_lens[b]
+ * counts them); its query, output, new-row and slot entries are the flat
+ * rows query_start[b] .. query_start[b+1] - 1. Query i attends to positions
+ * t <= L - n_b + i. The result equals pa_verify run on each sequence alone.
+ *
+ *   d_q, d_out     [total_queries, q_heads, head_dim], device.
+ *   d_k_new, d_v_new [total_queries, kv_heads, head_dim], device.
+ *   d_slot_mapping [total_queries] int32, device.
+ *   d_query_start  [batch + 1] int32, device: 0 = query_start[0] <= ... <=
+ *                  query_start[batch] = total_queries. An entry outside that
+ *                  order, or an n_b above max_queries, is clamped and raises
+ *                  PA_FLAG_BAD_LENGTH.
+ *   max_queries    host bound on every n_b (>= 1); the workspace is sized with
+ *                  it as num_queries (pa_workspace_size).
+ *   Other arguments as in pa_verify. PA_KERNEL_MMA_LDG is not supported here.
+ */
+pa_status pa_verify_ragged(const pa_cache *cache, const void *d_q, void *d_out, const void *d_k_new,
+                           const void *d_v_new, const int32_t *d_slot_mapping,
+                           const int32_t *d_query_start, int32_t total_queries, int32_t max_queries,
+                           const int32_t *d_block_tables, int32_t max_blocks_per_seq,
+                           const int32_t *d_context_lens, int32_t batch, int32_t q_heads,
+                           int32_t max_context_len, float scale, void *d_workspace,
+                           size_t workspace_bytes, const pa_options *opts, void *stream);
+
+/*
  * pa_validate: check the device-resident per-step inputs without attending.
  * Writes a report of PA_VALIDATE_WORDS uint32 words to d_report (device):
  *   [0] PA_FLAG_* bits found;

@@ -206,6 +206,38 @@ class Oracle:
                               scale, b_range)
 
 
+    # ---- ragged verify: a different number of new tokens per sequence ----
+
+    def verify_ragged(self, k_cache, v_cache, q, k_new, v_new, slot_mapping, query_start, block_tables,
+                      context_lens, scale, q8_scales=None):
+        """Write every new row (in place), then attend per sequence: sequence b's
+        n_b = query_start[b+1] - query_start[b] query tokens (flat rows of q) sit
+        at positions L_b - n_b + i, causal among themselves ("From 183 ms to
+        19 ms per decode step", section "Then speculative decoding got slower").
+        q8_scales = (k_scale, v_scale) for an int8 pool (k_cache / v_cache are
+        then the code bytes). Returns float64 [total, q_heads, head_dim]."""
+        qs = np.asarray(query_start, dtype=np.int64)
+        if q8_scales is None:
+            bad = self.cache_write(k_cache, v_cache, k_new, v_new, slot_mapping)
+        else:
+            bad = self.cache_write_q8(k_cache, v_cache, *q8_scales, k_new, v_new, slot_mapping)
+        if bad:
+            raise ValueError(f"oracle verify_ragged: {bad} out-of-range slot(s)")
+        out = np.zeros(q.shape, dtype=np.float64)
+        for b in range(len(context_lens)):
+            a, e = int(qs[b]), int(qs[b + 1])
+            if e == a:
+                continue
+            qb = np.ascontiguousarray(q[a:e][None])
+            tb = np.ascontiguousarray(block_tables[b:b + 1])
+            lb = np.ascontiguousarray(context_lens[b:b + 1])
+            if q8_scales is None:
+                out[a:e] = self.attend(k_cache, v_cache, qb, tb, lb, scale)[0]
+            else:
+                out[a:e] = self.decode_q8(k_cache, v_cache, *q8_scales, qb, tb, lb, scale)[0]
+        return out
+
+
 def _dtype_code(arr: np.ndarray) -> int:
     if arr.dtype == np.float32:
         return F32
@@ -268,6 +300,10 @@ def decode_q8(*args, **kwargs) -> np.ndarray:
 
 def verify_q8(*args, **kwargs) -> np.ndarray:
     return get().verify_q8(*args, **kwargs)
+
+
+def verify_ragged(*args, **kwargs) -> np.ndarray:
+    return get().verify_ragged(*args, **kwargs)
 
 
 def bf16_bits_to_f64(bits: np.ndarray) -> np.ndarray:

@@ -205,6 +205,39 @@ def pa_verify(k_cache, v_cache, q, k_new, v_new, slot_mapping, block_tables, con
     return out
 
 
+def pa_verify_ragged(k_cache, v_cache, q, k_new, v_new, slot_mapping, query_start, block_tables,
+                     context_lens, max_context_len: int, scale: float, workspace, max_queries: int,
+                     out=None, split_tokens: int = 0, kernel: str = "auto", stream=None, k_scale=None,
+                     v_scale=None):
+    """Verify with a different number of new tokens per sequence, in one launch.
+
+    q: [total, q_heads, head_dim]; sequence b owns rows query_start[b] ..
+    query_start[b+1] - 1 (int32 [batch + 1] on the device); max_queries bounds
+    every sequence's count (the workspace is sized with it as num_queries).
+    """
+    cache = make_cache(k_cache, v_cache, k_scale, v_scale)
+    _need(q.dim() == 3 and q.dtype == _row_dtype(k_cache) and q.is_contiguous(),
+          "q must be [total_queries, q_heads, head_dim] of the row dtype")
+    total, q_heads, _ = q.shape
+    batch = int(context_lens.shape[0])
+    mbps = _tables(block_tables, context_lens, batch)
+    _need(query_start.dtype == torch.int32 and query_start.shape == (batch + 1,) and query_start.is_contiguous(),
+          "query_start must be int32 [batch + 1]")
+    _need(slot_mapping.dtype == torch.int32 and slot_mapping.shape == (total,), "slot_mapping must be int32 [total]")
+    _need(k_new.shape == (total, cache.kv_heads, cache.head_dim) and k_new.shape == v_new.shape
+          and k_new.dtype == q.dtype and v_new.dtype == q.dtype,
+          "new rows must be [total_queries, kv_heads, head_dim] of the row dtype")
+    if out is None:
+        out = torch.empty_like(q)
+    opts = _options(split_tokens, kernel)
+    L.check("pa_verify_ragged", L.load().pa_verify_ragged(
+        ctypes.byref(cache), _vp(q), _vp(out), _vp(k_new), _vp(v_new), _vp(slot_mapping), _vp(query_start),
+        total, int(max_queries), _vp(block_tables), mbps, _vp(context_lens), batch, q_heads,
+        int(max_context_len), float(scale), _vp(workspace), workspace.numel() * workspace.element_size(),
+        ctypes.byref(opts), _stream(stream)))
+    return out
+
+
 def pa_validate(k_cache, v_cache, block_tables, context_lens, max_context_len: int,
                 slot_mapping=None, num_queries: int = 1, report=None, stream=None, k_scale=None,
                 v_scale=None):

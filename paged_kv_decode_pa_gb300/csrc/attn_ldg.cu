@@ -110,7 +110,7 @@ __global__ void __launch_bounds__(32 * W, ((NT == 1 && PF == 1) ? 12 : 8) / W)
     const int r = nt * 8 + ln.g;
     const bool live = r < nrows;
     const uint32_t* qrow = reinterpret_cast<const uint32_t*>(static_cast<const uint16_t*>(p.q) +
-                                                             row_offset(p, b, h, row0 + (live ? r : 0)));
+                                                             row_offset(p, int64_t(b) * p.num_queries, h, row0 + (live ? r : 0)));
 #pragma unroll
     for (int kk = 0; kk < 8; ++kk) {
       qb[kk][nt][0] = live ? __ldg(qrow + kk * 8 + ln.c) : 0u;
@@ -123,7 +123,7 @@ __global__ void __launch_bounds__(32 * W, ((NT == 1 && PF == 1) ? 12 : 8) / W)
 #pragma unroll
     for (int e = 0; e < 2; ++e) {
       const int r = nt * 8 + 2 * ln.c + e;
-      limit[nt][e] = r < nrows ? row_limit(p, L, row0 + r) : -1;
+      limit[nt][e] = r < nrows ? row_limit(p, L, p.num_queries, row0 + r) : -1;
     }
   __syncthreads();  // block ids visible
 
@@ -278,7 +278,7 @@ __global__ void __launch_bounds__(32 * W, ((NT == 1 && PF == 1) ? 12 : 8) / W)
         const int d = mt * 16 + ln.g + (e >> 1) * 8;
         if (r < nrows) {
           if (single) {
-            uint16_t* dst = static_cast<uint16_t*>(p.out) + row_offset(p, b, h, row0 + r) + d;
+            uint16_t* dst = static_cast<uint16_t*>(p.out) + row_offset(p, int64_t(b) * p.num_queries, h, row0 + r) + d;
             *dst = uint16_t(pack_bf16x2(val, 0.f) & 0xffffu);
           } else {
             p.part_o[(pslot * kRowSlots + r) * kHeadDim + d] = val;

@@ -99,6 +99,7 @@ __global__ void __launch_bounds__(kMmaThreads, NT == 1 ? 4 : 3)
       s_ids[j] = __ldg(p.block_tables + int64_t(b) * p.mbps + j0 + j);
   }
   const CtaWork w = cta_work(p, L_raw);
+  if (w.nrows <= 0) return;  // a ragged sequence with fewer query rows than this group
   if (w.split_size != p.split_tokens) {
     // A long sequence with its own split size: its entries start elsewhere.
     // Each thread rewrites the indices it wrote above, so no barrier is needed.
@@ -171,7 +172,7 @@ __global__ void __launch_bounds__(kMmaThreads, NT == 1 ? 4 : 3)
       const bool live = r < w.nrows;
       const uint32_t* qrow =
           reinterpret_cast<const uint32_t*>(static_cast<const uint16_t*>(p.q) +
-                                            row_offset(p, w.b, w.h, w.row0 + (live ? r : 0)));
+                                            row_offset(p, w.q0, w.h, w.row0 + (live ? r : 0)));
 #pragma unroll
       for (int kk = 0; kk < 8; ++kk) {
         qb[kk][nt][0] = live ? __ldg(qrow + kk * 8 + c) : 0u;
@@ -186,10 +187,10 @@ __global__ void __launch_bounds__(kMmaThreads, NT == 1 ? 4 : 3)
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
         const int r = nt * 8 + 2 * c + e;
-        limit[nt][e] = r < w.nrows ? row_limit(p, w.L, w.row0 + r) : -1;
+        limit[nt][e] = r < w.nrows ? row_limit(p, w.L, w.nq, w.row0 + r) : -1;
       }
 
-    const int new0 = w.L - p.num_queries;  // first position of a new (verify) token
+    const int new0 = w.L - w.nq;  // first position of a new (verify) token
 
     for (int j = warp; j < nblk; j += kMmaConsumers) {
       const int s = j % kStages;
@@ -217,12 +218,12 @@ __global__ void __launch_bounds__(kMmaThreads, NT == 1 ? 4 : 3)
           const int i = pos - new0;
           const int t = pos - tok0;
           const int64_t src =
-              (int64_t(w.b * p.num_queries + i) * p.kv_heads + w.h) * kHeadDim + ch * 8;
+              (int64_t(w.q0 + i) * p.kv_heads + w.h) * kHeadDim + ch * 8;
           const uint16_t* srcp = static_cast<const uint16_t*>(is_v ? p.v_new : p.k_new) + src;
           const uint4 val = __ldg(reinterpret_cast<const uint4*>(srcp));
           *reinterpret_cast<uint4*>((is_v ? vt_ptr : kt_ptr) + tile_off(t, ch)) = val;
           if (w.rg == 0) {
-            const int slot = __ldg(p.slot_mapping + w.b * p.num_queries + i);
+            const int slot = __ldg(p.slot_mapping + w.q0 + i);
             if (slot >= 0 && slot < p.num_blocks * kBlockSize) {
               const int64_t dst = ((int64_t(w.h) * p.num_blocks + slot / kBlockSize) * kBlockSize +
                                    slot % kBlockSize) * kHeadDim + ch * 8;

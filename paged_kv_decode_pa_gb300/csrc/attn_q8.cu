@@ -65,14 +65,14 @@ struct Q8Maps {
 // of the consumers' budget.
 __device__ __noinline__ void q8_fuse_new_rows(const AttnParams& p, const CtaWork& w, uint8_t* stp, int id,
                                               int tok0, int lane) {
-  const int new0 = w.L - p.num_queries;
+  const int new0 = w.L - w.nq;
   const int lo = max(tok0, new0), hi = min(tok0 + kBlockSize, w.L);
   const bool in_pool = id >= 0 && id < p.num_blocks;
 
   // Rows to write: lane t < 16 checks position tok0 + t.
   const int pos = tok0 + lane;
   const bool is_new = lane < kBlockSize && pos >= lo && pos < hi;
-  const int slot = is_new ? __ldg(p.slot_mapping + w.b * p.num_queries + (pos - new0)) : -1;
+  const int slot = is_new ? __ldg(p.slot_mapping + w.q0 + (pos - new0)) : -1;
   const bool ok = is_new && slot >= 0 && in_pool && slot == id * kBlockSize + lane;
   const uint32_t rows = __ballot_sync(0xffffffffu, ok);
   if (__any_sync(0xffffffffu, is_new && slot >= 0 && !ok) && lane == 0) raise_flag(p.status, PA_FLAG_BAD_SLOT);
@@ -88,7 +88,7 @@ __device__ __noinline__ void q8_fuse_new_rows(const AttnParams& p, const CtaWork
   float* vspool = static_cast<float*>(p.v_scale_w) + blk * kBlockSize;
   // Row t of this block is new token (tok0 + t - new0): its 4 channels of lane l.
   const int64_t row_step = int64_t(p.kv_heads) * kHeadDim;
-  const int64_t first = (int64_t(w.b * p.num_queries) + (tok0 - new0)) * row_step + int64_t(w.h) * kHeadDim + 4 * lane;
+  const int64_t first = (int64_t(w.q0) + (tok0 - new0)) * row_step + int64_t(w.h) * kHeadDim + 4 * lane;
   const uint2* knew = reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(p.k_new) + first);
   const uint2* vnew = reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(p.v_new) + first);
   const int64_t step2 = row_step / 4;  // in uint2 units
@@ -199,6 +199,7 @@ __global__ void __launch_bounds__(kQ8Threads, NT == 1 ? 5 : 3)
       s_ids[j] = __ldg(p.block_tables + int64_t(b) * p.mbps + j0 + j);
   }
   const CtaWork w = cta_work(p, L_raw);
+  if (w.nrows <= 0) return;  // a ragged sequence with fewer query rows than this group
   if (w.split_size != p.split_tokens) {
     // A long sequence with its own split size: its entries start elsewhere.
     // Each thread rewrites the indices it wrote above, so no barrier is needed.
@@ -234,24 +235,24 @@ __global__ void __launch_bounds__(kQ8Threads, NT == 1 ? 5 : 3)
   // since a single row group has at most 16 query tokens) are requantised by
   // the producer warp before their consumer attends over them.
   const int nmain =
-      p.fused_write ? min(nblk, max(0, (w.L - p.num_queries - w.t0) / kBlockSize)) : nblk;
+      p.fused_write ? min(nblk, max(0, (w.L - w.nq - w.t0) / kBlockSize)) : nblk;
 
   if (warp == kQ8Consumers) {
     // ---------------- producer ----------------
     if (nmain < nblk) {
       // The new tokens' rows and slots are needed only at the end of the
       // split: start bringing them into L2 now.
-      const int new0 = w.L - p.num_queries;
+      const int new0 = w.L - w.nq;
       for (int pos = max(new0, w.t0); pos < w.t1; ++pos) {
-        const int64_t row = (int64_t(w.b * p.num_queries + pos - new0) * p.kv_heads + w.h) * kHeadDim + 4 * lane;
+        const int64_t row = (int64_t(w.q0 + pos - new0) * p.kv_heads + w.h) * kHeadDim + 4 * lane;
         prefetch_l2(static_cast<const uint16_t*>(p.k_new) + row);
         prefetch_l2(static_cast<const uint16_t*>(p.v_new) + row);
       }
-      if (lane == 0) prefetch_l2(p.slot_mapping + w.b * p.num_queries);
+      if (lane == 0) prefetch_l2(p.slot_mapping + w.q0);
     }
     if (lane == 0) {
       const uint64_t policy = policy_evict_first();
-      const int new0 = w.L - p.num_queries;  // first position the append may have rewritten
+      const int new0 = w.L - w.nq;  // first position the append may have rewritten
       bool waited = !p.wait_append;
       int issued = 0;
       for (int j = 0; j < nblk; ++j) {
@@ -311,7 +312,7 @@ __global__ void __launch_bounds__(kQ8Threads, NT == 1 ? 5 : 3)
       for (int nt = 0; nt < NT; ++nt) {
         const int r = nt * 8 + g;
         live[nt] = r < w.nrows;
-        off[nt] = row_offset(p, w.b, w.h, w.row0 + (live[nt] ? r : 0));
+        off[nt] = row_offset(p, w.q0, w.h, w.row0 + (live[nt] ? r : 0));
       }
       q8_load_q<NT>(static_cast<const uint16_t*>(p.q), off, live, c, qb);
     }
@@ -321,7 +322,7 @@ __global__ void __launch_bounds__(kQ8Threads, NT == 1 ? 5 : 3)
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
         const int r = nt * 8 + 2 * c + e;
-        limit[nt][e] = r < w.nrows ? row_limit(p, w.L, w.row0 + r) : -1;
+        limit[nt][e] = r < w.nrows ? row_limit(p, w.L, w.nq, w.row0 + r) : -1;
       }
 
     // Blocks go in pairs (2p, 2p+1) to warp p % kQ8Consumers; a lone last

@@ -55,6 +55,7 @@ __global__ void __launch_bounds__(kSimtThreads) attn_simt_kernel(const AttnParam
   __shared__ int s_flag[4];
 
   const CtaWork w = cta_work(p);
+  if (w.nrows <= 0) return;  // a ragged sequence with fewer query rows than this group
   if (w.split >= w.nsplit) {
     if (w.L == 0 && w.split == 0) write_zero_rows<T>(p, w);
     return;
@@ -62,7 +63,7 @@ __global__ void __launch_bounds__(kSimtThreads) attn_simt_kernel(const AttnParam
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int d0 = lane * 4;
   const int nblk = (w.t1 - w.t0 + kBlockSize - 1) / kBlockSize;
-  const int new0 = w.L - p.num_queries;
+  const int new0 = w.L - w.nq;
   const T* kc = static_cast<const T*>(p.k_cache);
   const T* vc = static_cast<const T*>(p.v_cache);
 
@@ -71,8 +72,8 @@ __global__ void __launch_bounds__(kSimtThreads) attn_simt_kernel(const AttnParam
 #pragma unroll
   for (int r = 0; r < kSimtRows; ++r) {
     if (r < w.nrows) {
-      Vec4<T>::load(static_cast<const T*>(p.q) + row_offset(p, w.b, w.h, w.row0 + r) + d0, q[r]);
-      limit[r] = row_limit(p, w.L, w.row0 + r);
+      Vec4<T>::load(static_cast<const T*>(p.q) + row_offset(p, w.q0, w.h, w.row0 + r) + d0, q[r]);
+      limit[r] = row_limit(p, w.L, w.nq, w.row0 + r);
     } else {
       q[r][0] = q[r][1] = q[r][2] = q[r][3] = 0.f;
       limit[r] = -1;
@@ -94,11 +95,11 @@ __global__ void __launch_bounds__(kSimtThreads) attn_simt_kernel(const AttnParam
       if (p.fused_write && pos >= new0) {
         // A new (verify) token: read it from the inputs; row group 0 writes it.
         const int i = pos - new0;
-        const int64_t src = (int64_t(w.b * p.num_queries + i) * p.kv_heads + w.h) * kHeadDim + d0;
+        const int64_t src = (int64_t(w.q0 + i) * p.kv_heads + w.h) * kHeadDim + d0;
         Vec4<T>::load(static_cast<const T*>(p.k_new) + src, k);
         Vec4<T>::load(static_cast<const T*>(p.v_new) + src, v);
         if (w.rg == 0) {
-          const int slot = __ldg(p.slot_mapping + w.b * p.num_queries + i);
+          const int slot = __ldg(p.slot_mapping + w.q0 + i);
           if (slot >= 0 && slot < p.num_blocks * kBlockSize) {
             const int64_t dst =
                 ((int64_t(w.h) * p.num_blocks + slot / kBlockSize) * kBlockSize + slot % kBlockSize) *

@@ -36,7 +36,9 @@ __global__ void __launch_bounds__(kMergeWarps * 32) merge_kernel(const AttnParam
   const int bh = unit / p.row_groups;
   const int h = bh % p.kv_heads, b = bh / p.kv_heads;
   const int row0 = rg * p.rows_per_cta;
-  if (r >= min(p.rows_per_cta, p.rows - row0)) return;
+  int q0, nq;
+  seq_queries(p, b, false, &q0, &nq);
+  if (r >= min(p.rows_per_cta, nq * p.group - row0)) return;
   const int cap = min(p.max_context_len, p.mbps * kBlockSize);
   int L = __ldg(p.context_lens + b);
   L = L < 0 ? 0 : min(L, cap);
@@ -108,7 +110,7 @@ __global__ void __launch_bounds__(kMergeWarps * 32) merge_kernel(const AttnParam
     }
   }
   const float iv = den > 0.f ? 1.f / den : 0.f;
-  uint16_t* dst = static_cast<uint16_t*>(p.out) + row_offset(p, b, h, row0 + r) + lane * 4;
+  uint16_t* dst = static_cast<uint16_t*>(p.out) + row_offset(p, q0, h, row0 + r) + lane * 4;
   uint2 u;
   u.x = pack_bf16x2(acc.x * iv, acc.y * iv);
   u.y = pack_bf16x2(acc.z * iv, acc.w * iv);

@@ -238,11 +238,14 @@ __global__ void validate_kernel(const int32_t* __restrict__ tables, int32_t mbps
 }
 
 // Shared by pa_decode and pa_verify.
+// query_start: null for num_queries (nq) tokens per sequence; otherwise the
+// ragged layout ([batch + 1] offsets into total_queries tokens, at most nq per
+// sequence).
 pa_status attend(const pa_cache* cache, const void* q, void* out, const void* k_new,
                  const void* v_new, const int32_t* slots, int32_t nq, const int32_t* tables,
                  int32_t mbps, const int32_t* lens, int32_t batch, int32_t q_heads,
                  int32_t max_ctx, float scale, void* ws, size_t ws_bytes, const pa_options* opts,
-                 void* stream_ptr) {
+                 void* stream_ptr, const int32_t* query_start = nullptr, int32_t total_queries = 0) {
   pa_status st = check_cache(cache);
   if (st != PA_OK) return st;
   if (batch < 0 || max_ctx < 0 || nq < 1 || q_heads <= 0) return PA_ERR_INVALID_ARG;
@@ -258,6 +261,7 @@ pa_status attend(const pa_cache* cache, const void* q, void* out, const void* k_
   if (kernel == PA_KERNEL_AUTO) kernel = bf16 ? PA_KERNEL_MMA : PA_KERNEL_SIMT;
   const bool use_mma = kernel == PA_KERNEL_MMA || kernel == PA_KERNEL_MMA_LDG;
   if (use_mma && !bf16) return PA_ERR_UNSUPPORTED;
+  if (query_start && kernel == PA_KERNEL_MMA_LDG) return PA_ERR_UNSUPPORTED;
   const int32_t prefetch = (opts && opts->prefetch > 0) ? opts->prefetch : PA_DEFAULT_PREFETCH;
   if (prefetch > 2) return PA_ERR_UNSUPPORTED;
   const int32_t warps = (opts && opts->warps > 0) ? opts->warps : PA_DEFAULT_WARPS;
@@ -286,6 +290,8 @@ pa_status attend(const pa_cache* cache, const void* q, void* out, const void* k_
   p.k_new = k_new;
   p.v_new = v_new;
   p.slot_mapping = slots;
+  p.query_start = query_start;
+  p.total_queries = query_start ? total_queries : batch * nq;
   p.block_tables = tables;
   p.context_lens = lens;
   uint8_t* wsb = static_cast<uint8_t*>(ws);
@@ -334,7 +340,7 @@ pa_status attend(const pa_cache* cache, const void* q, void* out, const void* k_
     p.fused_write = (fused && !append_first) ? 1 : 0;
     p.wait_append = append_first ? 1 : 0;
     e = cudaSuccess;
-    if (append_first) e = launch_cache_write_q8(cache, k_new, v_new, slots, batch * nq, p.status, stream);
+    if (append_first) e = launch_cache_write_q8(cache, k_new, v_new, slots, p.total_queries, p.status, stream);
     if (e == cudaSuccess) e = launch_attn_q8(maps, p, grid, append_first, stream);
     if (e == cudaSuccess && p.max_splits > 1) e = launch_merge(p, stream);
   } else if (kernel == PA_KERNEL_MMA_LDG) {
@@ -443,6 +449,21 @@ pa_status pa_verify(const pa_cache* cache, const void* q, void* out, const void*
   return attend(cache, q, out, k_new, v_new, slot_mapping, num_queries, block_tables,
                 max_blocks_per_seq, context_lens, batch, q_heads, max_context_len, scale, workspace,
                 workspace_bytes, opts, stream);
+}
+
+pa_status pa_verify_ragged(const pa_cache* cache, const void* q, void* out, const void* k_new,
+                           const void* v_new, const int32_t* slot_mapping, const int32_t* query_start,
+                           int32_t total_queries, int32_t max_queries, const int32_t* block_tables,
+                           int32_t max_blocks_per_seq, const int32_t* context_lens, int32_t batch,
+                           int32_t q_heads, int32_t max_context_len, float scale, void* workspace,
+                           size_t workspace_bytes, const pa_options* opts, void* stream) {
+  if (total_queries < 0 || max_queries < 1 || batch < 0) return PA_ERR_INVALID_ARG;
+  if (batch > 0 && !query_start) return PA_ERR_INVALID_ARG;
+  if (batch == 0 || total_queries == 0) return check_cache(cache);
+  if (!k_new || !v_new || !slot_mapping) return PA_ERR_INVALID_ARG;
+  return attend(cache, q, out, k_new, v_new, slot_mapping, max_queries, block_tables, max_blocks_per_seq,
+                context_lens, batch, q_heads, max_context_len, scale, workspace, workspace_bytes, opts,
+                stream, query_start, total_queries);
 }
 
 pa_status pa_validate(const pa_cache* cache, const int32_t* block_tables, int32_t max_blocks_per_seq,

@@ -36,14 +36,16 @@ struct AttnParams {
   const void* k_new;  // [batch * num_queries, kv_heads, 128] (fused verify only)
   const void* v_new;
   const int32_t* slot_mapping;  // [batch * num_queries] (fused verify only)
+  const int32_t* query_start;   // ragged: [batch + 1] first query token of each sequence; null: uniform
+  int32_t total_queries;        // ragged: query tokens in all (rows of q / out / k_new / v_new)
   const int32_t* block_tables;  // [batch, mbps]
   const int32_t* context_lens;  // [batch]
   uint32_t* status;             // workspace status word
   int32_t* counters;            // one per (sequence, kv head, row group)
   float* part_lse;              // [units, max_splits, 16]       (log2 units)
   float* part_o;                // [units, max_splits, 16, 128]
-  int32_t kv_heads, num_blocks, mbps, batch, q_heads, group, num_queries;
-  int32_t rows;        // num_queries * group: query rows per (sequence, kv head)
+  int32_t kv_heads, num_blocks, mbps, batch, q_heads, group, num_queries;  // ragged: the most of any sequence
+  int32_t rows;        // num_queries * group: query rows per (sequence, kv head), at most
   int32_t rows_per_cta;  // 16 (tensor-core kernel) or 8 (CUDA-core kernel)
   int32_t row_groups;  // ceil(rows / rows_per_cta)
   int32_t max_context_len, split_tokens, max_splits;
@@ -213,9 +215,30 @@ struct CtaWork {
   int nsplit;     // non-empty splits of this sequence
   int t0, t1;     // token range of this split
   int row0;       // first row of this row group
-  int nrows;      // rows of this group (<= rows_per_cta)
+  int nrows;      // rows of this group (<= rows_per_cta; <= 0: none)
   int unit;       // (b * kv_heads + h) * row_groups + rg
+  int nq;         // this sequence's query tokens (new tokens at L - nq .. L - 1)
+  int q0;         // flat index of its first query token (q, out, k_new, v_new, slots)
 };
+
+// Query tokens of sequence b: uniform (num_queries each) or from query_start
+// (clamped to [0, num_queries] and to the flat arrays; an inconsistent entry
+// raises PA_FLAG_BAD_LENGTH once).
+__device__ __forceinline__ void seq_queries(const AttnParams& p, int b, bool report, int* q0, int* nq) {
+  if (!p.query_start) {
+    *q0 = b * p.num_queries;
+    *nq = p.num_queries;
+    return;
+  }
+  const int a = __ldg(p.query_start + b), e = __ldg(p.query_start + b + 1);
+  int s = max(0, min(a, p.total_queries)), n = max(0, min(e, p.total_queries) - s);
+  if (n > p.num_queries || a < 0 || e < a || e > p.total_queries) {
+    if (report) raise_flag(p.status, PA_FLAG_BAD_LENGTH);
+    n = min(n, p.num_queries);
+  }
+  *q0 = s;
+  *nq = n;
+}
 
 // The work of CTA (blockIdx.x = split, .y = KV head, .z = sequence x row
 // group); L_raw is context_lens[b] if the caller has loaded it already.
@@ -225,6 +248,7 @@ __device__ __forceinline__ CtaWork cta_work(const AttnParams& p, int L_raw = -21
   w.h = blockIdx.y;
   w.b = blockIdx.z / p.row_groups;
   w.rg = blockIdx.z - w.b * p.row_groups;
+  seq_queries(p, w.b, w.split == 0 && w.h == 0 && w.rg == 0, &w.q0, &w.nq);
   int L = L_raw == -2147483647 - 1 ? __ldg(p.context_lens + w.b) : L_raw;
   const int cap = min(p.max_context_len, p.mbps * kBlockSize);
   if (L < 0 || L > cap) {
@@ -237,21 +261,22 @@ __device__ __forceinline__ CtaWork cta_work(const AttnParams& p, int L_raw = -21
   w.t0 = w.split * w.split_size;
   w.t1 = min(L, w.t0 + w.split_size);
   w.row0 = w.rg * p.rows_per_cta;
-  w.nrows = min(p.rows_per_cta, p.rows - w.row0);
+  w.nrows = min(p.rows_per_cta, w.nq * p.group - w.row0);
   w.unit = (w.b * p.kv_heads + w.h) * p.row_groups + w.rg;
   return w;
 }
 
-// Element offset of query row r (r = i * group + g) of sequence b, kv head h.
-__device__ __forceinline__ int64_t row_offset(const AttnParams& p, int b, int h, int r) {
+// Element offset of query row r (r = i * group + g) of kv head h, for the
+// sequence whose first query token is q0.
+__device__ __forceinline__ int64_t row_offset(const AttnParams& p, int64_t q0, int h, int r) {
   const int i = r / p.group;
   const int g = r - i * p.group;
-  return ((int64_t(b) * p.num_queries + i) * p.q_heads + h * p.group + g) * kHeadDim;
+  return ((q0 + i) * p.q_heads + h * p.group + g) * kHeadDim;
 }
 
-// Last position query row r may attend to (causal among the new tokens).
-__device__ __forceinline__ int row_limit(const AttnParams& p, int L, int r) {
-  return L - p.num_queries + r / p.group;
+// Last position query row r may attend to (causal among the sequence's nq new tokens).
+__device__ __forceinline__ int row_limit(const AttnParams& p, int L, int nq, int r) {
+  return L - nq + r / p.group;
 }
 
 template <typename T>
@@ -279,7 +304,7 @@ __device__ void write_zero_rows(const AttnParams& p, const CtaWork& w) {
   const float z[8] = {0, 0, 0, 0, 0, 0, 0, 0};
   for (int e = threadIdx.x; e < w.nrows * (kHeadDim / 8); e += blockDim.x) {
     const int r = e / (kHeadDim / 8), c = e % (kHeadDim / 8);
-    T* dst = static_cast<T*>(p.out) + row_offset(p, w.b, w.h, w.row0 + r) + c * 8;
+    T* dst = static_cast<T*>(p.out) + row_offset(p, w.q0, w.h, w.row0 + r) + c * 8;
     store8<T>(dst, z);
   }
 }
@@ -321,7 +346,7 @@ __device__ void split_epilogue(const AttnParams& p, const CtaWork& w, const floa
 #pragma unroll
     for (int d = 0; d < 8; ++d) acc[d] *= inv;
     if (single) {
-      T* dst = static_cast<T*>(p.out) + row_offset(p, w.b, w.h, w.row0 + r) + c * 8;
+      T* dst = static_cast<T*>(p.out) + row_offset(p, w.q0, w.h, w.row0 + r) + c * 8;
       store8<T>(dst, acc);
     } else {
       float* dst = p.part_o + (slot * kRowSlots + r) * kHeadDim + c * 8;
@@ -369,7 +394,7 @@ __device__ void split_epilogue(const AttnParams& p, const CtaWork& w, const floa
     const float inv = den > 0.f ? 1.f / den : 0.f;
 #pragma unroll
     for (int d = 0; d < 8; ++d) acc[d] *= inv;
-    T* dst = static_cast<T*>(p.out) + row_offset(p, w.b, w.h, w.row0 + r) + c * 8;
+    T* dst = static_cast<T*>(p.out) + row_offset(p, w.q0, w.h, w.row0 + r) + c * 8;
     store8<T>(dst, acc);
   }
   if (threadIdx.x == 0) p.counters[w.unit] = 0;

@@ -278,3 +278,35 @@ def q8_pool(w: Workload, seed: Optional[int] = None) -> Q8Pool:
     vs = np.full((hkv, nb, bs), np.nan, dtype=np.float32)
     vs[:, held] = rng.uniform(0.005, 0.05, size=(hkv, int(held.sum()))).astype(np.float32)
     return Q8Pool(kq, vq, ks, vs)
+
+
+@dataclass
+class RaggedWorkload:
+    """A step whose sequences carry different numbers of new tokens."""
+    base: Workload             # the uniform workload it is cut from (num_queries = the most)
+    nq: np.ndarray             # [batch] new tokens of each sequence
+    query_start: np.ndarray    # [batch + 1] int32
+    q: np.ndarray              # [total, q_heads, head_dim]
+    k_new: np.ndarray          # [total, kv_heads, head_dim]
+    v_new: np.ndarray
+    slot_mapping: np.ndarray   # [total] int32
+
+    @property
+    def max_queries(self) -> int:
+        return int(self.nq.max()) if self.nq.size else 1
+
+
+def ragged(w: Workload, nq_per_seq) -> RaggedWorkload:
+    """Keep, for sequence b, the last nq_per_seq[b] of a uniform verify
+    workload's new tokens (those at positions L - n_b .. L - 1). A decode
+    sequence keeps one; zero keeps none."""
+    nq_max = w.spec.num_queries
+    n = np.asarray(nq_per_seq, dtype=np.int64)
+    assert n.shape == (w.spec.batch,) and n.min() >= 0 and n.max() <= nq_max
+    q4 = w.q if w.q.ndim == 4 else w.q[:, None]
+    rows = [b * nq_max + i for b in range(w.spec.batch) for i in range(nq_max - int(n[b]), nq_max)]
+    qs = np.concatenate([[0], np.cumsum(n)]).astype(np.int32)
+    q = q4.reshape(-1, *q4.shape[2:])[rows]
+    return RaggedWorkload(base=w, nq=n.astype(np.int32), query_start=qs, q=np.ascontiguousarray(q),
+                          k_new=np.ascontiguousarray(w.k_new[rows]), v_new=np.ascontiguousarray(w.v_new[rows]),
+                          slot_mapping=np.ascontiguousarray(w.slot_mapping[rows]))

@@ -431,10 +431,46 @@ def pin_q8_lossless_attention(orc):
     assert np.array_equal(got, ref)
 
 
+def pin_ragged_verify(orc):
+    """Ragged verify reduces to the pinned uniform verify: with the same count
+    for every sequence it is bit-identical to it, and in a mix each sequence's
+    rows (and the written pool) equal a uniform verify of that sequence alone
+    with its own count."""
+    w = inputs.custom(batch=5, q_heads=6, kv_heads=2, context_lens=(9, 20, 33, 16, 47), num_blocks=20,
+                      seed=31, num_queries=4)
+    same = inputs.ragged(w, [4] * 5)
+    kc, vc = w.k_cache.copy(), w.v_cache.copy()
+    got = orc.verify_ragged(kc, vc, same.q, same.k_new, same.v_new, same.slot_mapping, same.query_start,
+                            w.block_tables, w.context_lens, w.scale)
+    kr, vr = w.k_cache.copy(), w.v_cache.copy()
+    ref = orc.verify(kr, vr, w.q, w.k_new, w.v_new, w.slot_mapping, w.block_tables, w.context_lens, w.scale)
+    assert np.array_equal(got, ref.reshape(got.shape)) and kc.tobytes() == kr.tobytes()
+    mix = inputs.ragged(w, [1, 4, 0, 2, 3])
+    kc, vc = w.k_cache.copy(), w.v_cache.copy()
+    got = orc.verify_ragged(kc, vc, mix.q, mix.k_new, mix.v_new, mix.slot_mapping, mix.query_start,
+                            w.block_tables, w.context_lens, w.scale)
+    for b, n in enumerate(mix.nq):
+        if n == 0:
+            continue
+        a = int(mix.query_start[b])
+        one = inputs.custom(batch=1, q_heads=6, kv_heads=2, context_lens=(int(w.context_lens[b]),),
+                            num_blocks=20, seed=31, num_queries=int(n))
+        ka, va = w.k_cache.copy(), w.v_cache.copy()
+        refb = orc.verify(ka, va, mix.q[a:a + n][None], mix.k_new[a:a + n], mix.v_new[a:a + n],
+                          mix.slot_mapping[a:a + n], w.block_tables[b:b + 1], w.context_lens[b:b + 1], w.scale)
+        assert one.spec.num_queries == n
+        assert np.array_equal(got[a:a + n], refb[0])
+    # every sequence's written rows land in the pool (none is dropped)
+    kr, vr = w.k_cache.copy(), w.v_cache.copy()
+    orc.cache_write(kr, vr, mix.k_new, mix.v_new, mix.slot_mapping)
+    assert kc.tobytes() == kr.tobytes() and vc.tobytes() == vr.tobytes()
+
+
 ALL_PINS = [pin_bruteforce, pin_sdpa, pin_onehot_softmax, pin_constant_v, pin_single_token,
             pin_two_token_closed_form, pin_block_permutation, pin_gqa_repeat, pin_verify_rows,
             pin_zero_length, pin_cache_write, pin_q8_row_closed_form, pin_q8_requant_closed_form,
-            pin_q8_zero_and_partial_block, pin_q8_error_bound, pin_q8_lossless_attention]
+            pin_q8_zero_and_partial_block, pin_q8_error_bound, pin_q8_lossless_attention,
+            pin_ragged_verify]
 
 
 if __name__ == "__main__":

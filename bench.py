@@ -454,6 +454,60 @@ def measure_graph_buckets(device, flush, steps: int = 20) -> dict:
     return out
 
 
+def prefill_flops(context_lens, chunks, q_heads: int, head_dim: int = 128) -> int:
+    """Tensor-core flops of a causal prefill: each query row's score and value
+    products over its visible positions, 2 * head_dim each."""
+    f = 0
+    for L, n in zip(context_lens, chunks):
+        vis = np.arange(int(L) - int(n), int(L)) + 1
+        f += int(np.maximum(vis, 0).sum()) * q_heads * 4 * head_dim
+    return f
+
+
+def measure_prefill(device, flush, steps: int = 10) -> dict:
+    """Paged prefill (next row 2): the 64-request workload's prompts (64 x 256
+    tokens, 16/8 heads, no prefix) and a long chunk (8 sequences, 2048 tokens
+    after a 2048-token prefix, 12/2 heads); tensor-bound, reported against the
+    measured bf16 peak."""
+    import torch
+
+    import paged_kv_decode_pa_gb300 as pa
+
+    out = {}
+    peak = None
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            peak = float(json.load(f)["bf16_tflops"])
+    except Exception:
+        peak = 1900.0
+    for name, lens, chunks, hq, hkv, nb in (("prefill_64x256", (256,) * 64, (256,) * 64, 16, 8, 1100),
+                                              ("prefill_8x2048_after_2048", (4096,) * 8, (2048,) * 8, 12, 2, 2100)):
+        w = inputs.custom(batch=len(lens), q_heads=hq, kv_heads=hkv, context_lens=lens, num_blocks=nb, seed=61,
+                          num_queries=max(chunks))
+        rw = inputs.ragged(w, list(chunks))
+        kc, vc = pa.to_torch(w.k_cache, device), pa.to_torch(w.v_cache, device)
+        q, qs = pa.to_torch(rw.q, device), pa.to_torch(rw.query_start, device)
+        tb, ln = pa.to_torch(w.block_tables, device), pa.to_torch(w.context_lens, device)
+        o = torch.empty_like(q)
+        ts = []
+        for k in range(steps + 3):
+            flush()
+            gpu_hold()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            pa.pa_prefill(kc, vc, q, qs, tb, ln, w.max_context_len, w.scale, rw.max_queries, out=o)
+            e1.record()
+            torch.cuda.synchronize()
+            if k >= 3:
+                ts.append(e0.elapsed_time(e1))
+        us = statistics.mean(ts) * 1e3
+        fl = prefill_flops(lens, chunks, hq)
+        out[name] = {"us_per_call": round(us, 2), "gflop": round(fl / 1e9, 2),
+                     "tflops": round(fl / (us * 1e-6) / 1e12, 1), "bound": "tensor",
+                     "frac_of_measured_bf16": round(fl / (us * 1e-6) / 1e12 / peak, 3)}
+    return out
+
+
 def launches_per_step(w, step, split: int, kernel: str, kv: str) -> int:
     """libpa kernels one step launches: the append when it is not fused, the
     attention kernel, the log-sum-exp merge when a call has several splits
@@ -554,6 +608,7 @@ def run_native(args):
                                             args.prefetch, args.warps, not args.unfused, args.graph)
         if args.buckets:
             extra["graph_buckets_c2"] = measure_graph_buckets(device, flush)
+        extra.update(measure_prefill(device, flush))
         # The int8 pool (the next row of the scope): the same workloads with
         # dequantisation fused into the attention kernel.
         for name in ("c4", "c3", "c5"):

@@ -294,6 +294,31 @@ pa_status pa_verify_ragged(const pa_cache *cache, const void *d_q, void *d_out, 
                            size_t workspace_bytes, const pa_options *opts, void *stream);
 
 /*
+ * pa_prefill: causal attention of prompt chunks over the paged cache (prefill
+ * or chunked prefill; "From 183 ms to 19 ms per decode step", section "What's
+ * next"). Sequence b's chunk is its last n_b = query_start[b+1] -
+ * query_start[b] positions, L - n_b .. L - 1 (L = context_lens[b] counts
+ * them); their K/V must already be in the cache (pa_cache_write). Query token
+ * i of the chunk attends to positions t <= L - n_b + i; a token at a negative
+ * position gets zeros. Each K/V block is read once per 128 query rows (token x
+ * query head of one KV head).
+ *
+ *   cache          bf16 only (PA_ERR_UNSUPPORTED otherwise).
+ *   d_q, d_out     [total_queries, q_heads, head_dim] bf16, device.
+ *   d_query_start  [batch + 1] int32, device, as in pa_verify_ragged;
+ *                  max_queries bounds every n_b (it sizes the grid).
+ *   d_workspace    optional (NULL: no status word): a 256-byte-aligned buffer of
+ *                  >= 256 bytes whose first word receives PA_FLAG_* bits.
+ *   Other arguments as in pa_decode. No split-K: one CTA reads the whole
+ *   visible context of its 128 rows.
+ */
+pa_status pa_prefill(const pa_cache *cache, const void *d_q, void *d_out, const int32_t *d_query_start,
+                     int32_t total_queries, int32_t max_queries, const int32_t *d_block_tables,
+                     int32_t max_blocks_per_seq, const int32_t *d_context_lens, int32_t batch, int32_t q_heads,
+                     int32_t max_context_len, float scale, void *d_workspace, size_t workspace_bytes,
+                     void *stream);
+
+/*
  * pa_validate: check the device-resident per-step inputs without attending.
  * Writes a report of PA_VALIDATE_WORDS uint32 words to d_report (device):
  *   [0] PA_FLAG_* bits found;

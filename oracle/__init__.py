@@ -216,13 +216,22 @@ class Oracle:
         19 ms per decode step", section "Then speculative decoding got slower").
         q8_scales = (k_scale, v_scale) for an int8 pool (k_cache / v_cache are
         then the code bytes). Returns float64 [total, q_heads, head_dim]."""
-        qs = np.asarray(query_start, dtype=np.int64)
         if q8_scales is None:
             bad = self.cache_write(k_cache, v_cache, k_new, v_new, slot_mapping)
         else:
             bad = self.cache_write_q8(k_cache, v_cache, *q8_scales, k_new, v_new, slot_mapping)
         if bad:
             raise ValueError(f"oracle verify_ragged: {bad} out-of-range slot(s)")
+        return self.attend_ragged(k_cache, v_cache, q, query_start, block_tables, context_lens, scale, q8_scales)
+
+    def attend_ragged(self, k_cache, v_cache, q, query_start, block_tables, context_lens, scale,
+                      q8_scales=None):
+        """Attention only (nothing written): sequence b's query_start[b+1] -
+        query_start[b] flat q rows are its last positions, causal among
+        themselves. This is prefill / chunked prefill over a cache that already
+        holds the chunk ("From 183 ms to 19 ms per decode step", section
+        "What's next"). Returns float64 [total, q_heads, head_dim]."""
+        qs = np.asarray(query_start, dtype=np.int64)
         out = np.zeros(q.shape, dtype=np.float64)
         for b in range(len(context_lens)):
             a, e = int(qs[b]), int(qs[b + 1])
@@ -304,6 +313,10 @@ def verify_q8(*args, **kwargs) -> np.ndarray:
 
 def verify_ragged(*args, **kwargs) -> np.ndarray:
     return get().verify_ragged(*args, **kwargs)
+
+
+def attend_ragged(*args, **kwargs) -> np.ndarray:
+    return get().attend_ragged(*args, **kwargs)
 
 
 def bf16_bits_to_f64(bits: np.ndarray) -> np.ndarray:

@@ -42,7 +42,7 @@ PA_NOALLOC_SCRATCH_BYTES = 16 << 20
 
 # Every symbol include/pa.h declares.
 EXPORTED = ("pa_cache_write", "pa_workspace_size", "pa_workspace_init", "pa_workspace_status",
-            "pa_decode", "pa_verify", "pa_verify_ragged", "pa_validate", "pa_decode_noalloc",
+            "pa_decode", "pa_verify", "pa_verify_ragged", "pa_prefill", "pa_validate", "pa_decode_noalloc",
             "pa_status_string",
             "pa_last_cuda_error", "pa_version")
 
@@ -102,6 +102,8 @@ def load(path: Path | None = None):
                                      ctypes.c_float, vp, ctypes.c_size_t, opts_p, vp]),
         "pa_verify_ragged": (ctypes.c_int, [cache_p, vp, vp, vp, vp, vp, vp, i32, i32, vp, i32, vp, i32, i32,
                                             i32, ctypes.c_float, vp, ctypes.c_size_t, opts_p, vp]),
+        "pa_prefill": (ctypes.c_int, [cache_p, vp, vp, vp, i32, i32, vp, i32, vp, i32, i32, i32,
+                                      ctypes.c_float, vp, ctypes.c_size_t, vp]),
         "pa_validate": (ctypes.c_int, [cache_p, vp, i32, vp, i32, i32, vp, i32, vp, vp]),
         "pa_decode_noalloc": (ctypes.c_int, [cache_p, vp, vp, vp, i32, vp, i32, i32, i32,
                                              ctypes.c_float, opts_p, vp]),

@@ -238,6 +238,30 @@ def pa_verify_ragged(k_cache, v_cache, q, k_new, v_new, slot_mapping, query_star
     return out
 
 
+def pa_prefill(k_cache, v_cache, q, query_start, block_tables, context_lens, max_context_len: int,
+               scale: float, max_queries: int, out=None, workspace=None, stream=None):
+    """Causal attention of each sequence's prompt chunk (its last n_b positions,
+    already in the cache) over its paged context. q: [total, q_heads, head_dim]
+    bf16; query_start: int32 [batch + 1]. workspace (optional) receives the
+    status word."""
+    cache = make_cache(k_cache, v_cache)
+    _need(q.dim() == 3 and q.dtype == k_cache.dtype and q.is_contiguous(),
+          "q must be [total_queries, q_heads, head_dim] of the cache dtype")
+    total, q_heads, _ = q.shape
+    batch = int(context_lens.shape[0])
+    mbps = _tables(block_tables, context_lens, batch)
+    _need(query_start.dtype == torch.int32 and query_start.shape == (batch + 1,) and query_start.is_contiguous(),
+          "query_start must be int32 [batch + 1]")
+    if out is None:
+        out = torch.empty_like(q)
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    L.check("pa_prefill", L.load().pa_prefill(
+        ctypes.byref(cache), _vp(q), _vp(out), _vp(query_start), total, int(max_queries), _vp(block_tables),
+        mbps, _vp(context_lens), batch, q_heads, int(max_context_len), float(scale), _vp(workspace), ws_bytes,
+        _stream(stream)))
+    return out
+
+
 def pa_validate(k_cache, v_cache, block_tables, context_lens, max_context_len: int,
                 slot_mapping=None, num_queries: int = 1, report=None, stream=None, k_scale=None,
                 v_scale=None):

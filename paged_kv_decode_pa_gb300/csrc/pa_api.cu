@@ -23,6 +23,9 @@ cudaError_t launch_attn_q8(const Q8Maps& maps, const AttnParams& p, dim3 grid, b
                            cudaStream_t stream);
 cudaError_t launch_cache_write_q8(const pa_cache* c, const void* k_new, const void* v_new,
                                   const int32_t* slots, int32_t n, uint32_t* status, cudaStream_t stream);
+cudaError_t launch_attn_prefill(const CUtensorMap& tk, const CUtensorMap& tv, const AttnParams& p, dim3 grid,
+                                cudaStream_t stream);
+constexpr int kPrefillRows = 128;  // query rows per prefill CTA
 }  // namespace pa
 
 namespace {
@@ -464,6 +467,62 @@ pa_status pa_verify_ragged(const pa_cache* cache, const void* q, void* out, cons
   return attend(cache, q, out, k_new, v_new, slot_mapping, max_queries, block_tables, max_blocks_per_seq,
                 context_lens, batch, q_heads, max_context_len, scale, workspace, workspace_bytes, opts,
                 stream, query_start, total_queries);
+}
+
+pa_status pa_prefill(const pa_cache* cache, const void* q, void* out, const int32_t* query_start,
+                     int32_t total_queries, int32_t max_queries, const int32_t* block_tables,
+                     int32_t max_blocks_per_seq, const int32_t* context_lens, int32_t batch, int32_t q_heads,
+                     int32_t max_context_len, float scale, void* workspace, size_t workspace_bytes,
+                     void* stream) {
+  pa_status st = check_cache(cache);
+  if (st != PA_OK) return st;
+  if (cache->dtype != PA_DTYPE_BF16) return PA_ERR_UNSUPPORTED;
+  if (batch < 0 || total_queries < 0 || max_queries < 1 || max_context_len < 0 || q_heads <= 0)
+    return PA_ERR_INVALID_ARG;
+  if (q_heads % cache->kv_heads || !std::isfinite(scale)) return PA_ERR_INVALID_ARG;
+  if (batch == 0 || total_queries == 0) return PA_OK;
+  if (!q || !out || !query_start || !block_tables || !context_lens || !aligned16(q) || !aligned16(out))
+    return PA_ERR_INVALID_ARG;
+  if (max_blocks_per_seq <= 0 || int64_t(max_context_len) > int64_t(max_blocks_per_seq) * kBlockSize)
+    return PA_ERR_INVALID_ARG;
+  if (workspace && ((reinterpret_cast<uintptr_t>(workspace) & 255u) || workspace_bytes < 256))
+    return PA_ERR_WORKSPACE;
+  if (batch > 65535) return PA_ERR_UNSUPPORTED;
+  const int64_t rows = int64_t(max_queries) * (q_heads / cache->kv_heads);
+  const int64_t tiles = (rows + kPrefillRows - 1) / kPrefillRows;
+  if (tiles > INT32_MAX) return PA_ERR_UNSUPPORTED;
+
+  AttnParams p;
+  std::memset(&p, 0, sizeof p);
+  p.k_cache = cache->k;
+  p.v_cache = cache->v;
+  p.q = q;
+  p.out = out;
+  p.block_tables = block_tables;
+  p.context_lens = context_lens;
+  p.query_start = query_start;
+  p.total_queries = total_queries;
+  p.status = static_cast<uint32_t*>(workspace);
+  p.kv_heads = cache->kv_heads;
+  p.num_blocks = cache->num_blocks;
+  p.mbps = max_blocks_per_seq;
+  p.batch = batch;
+  p.q_heads = q_heads;
+  p.group = q_heads / cache->kv_heads;
+  p.num_queries = max_queries;
+  p.rows = int32_t(std::min<int64_t>(rows, INT32_MAX));
+  p.rows_per_cta = kPrefillRows;
+  p.row_groups = int32_t(tiles);
+  p.max_context_len = max_context_len;
+  p.split_tokens = kBlockSize;  // unused: a prefill CTA reads its rows' whole visible context
+  p.scale_log2 = scale * 1.4426950408889634f;
+  CUtensorMap tk, tv;
+  if (!make_pool_map(&tk, cache->k, cache->kv_heads, cache->num_blocks) ||
+      !make_pool_map(&tv, cache->v, cache->kv_heads, cache->num_blocks))
+    return cuda_fail(cudaErrorInvalidValue);
+  const dim3 grid(unsigned(tiles), unsigned(cache->kv_heads), unsigned(batch));
+  const cudaError_t e = launch_attn_prefill(tk, tv, p, grid, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? PA_OK : cuda_fail(e);
 }
 
 pa_status pa_validate(const pa_cache* cache, const int32_t* block_tables, int32_t max_blocks_per_seq,

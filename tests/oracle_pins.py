@@ -466,11 +466,40 @@ def pin_ragged_verify(orc):
     assert kc.tobytes() == kr.tobytes() and vc.tobytes() == vr.tobytes()
 
 
+def pin_prefill_sdpa(orc):
+    """Prefill (attention of each sequence's last n_b positions over a cache that
+    holds them) against torch's float64 scaled_dot_product_attention with the
+    causal mask offset by the prefix, over the gathered, repeat_kv-expanded
+    context; and n_b = 1 everywhere reduces to decode, bit for bit."""
+    import torch
+    import torch.nn.functional as F
+
+    lens = (1, 37, 80, 129, 16)
+    w = inputs.custom(batch=5, q_heads=12, kv_heads=2, context_lens=lens, num_blocks=40, seed=41, num_queries=33)
+    rw = inputs.ragged(w, [1, 33, 17, 20, 16])
+    got = orc.attend_ragged(w.k_cache, w.v_cache, rw.q, rw.query_start, w.block_tables, w.context_lens, w.scale)
+    bs, group = w.k_cache.shape[2], 6
+    for b, L in enumerate(lens):
+        a, e = int(rw.query_start[b]), int(rw.query_start[b + 1])
+        n = e - a
+        K = torch.from_numpy(_gather(w.k_cache, w.block_tables[b], L, bs)).repeat_interleave(group, 0)
+        V = torch.from_numpy(_gather(w.v_cache, w.block_tables[b], L, bs)).repeat_interleave(group, 0)
+        Q = torch.from_numpy(oracle.to_f64(rw.q[a:e])).transpose(0, 1)  # [Hq, n, D]
+        mask = torch.arange(L)[None, :] <= torch.arange(L - n, L)[:, None]
+        ref = F.scaled_dot_product_attention(Q, K, V, attn_mask=mask, scale=w.scale).transpose(0, 1).numpy()
+        err = np.max(np.abs(got[a:e] - ref))
+        assert err <= 1e-12, f"prefill sdpa mismatch {err}, seq {b}"
+    one = inputs.ragged(w, [1] * 5)
+    got1 = orc.attend_ragged(w.k_cache, w.v_cache, one.q, one.query_start, w.block_tables, w.context_lens, w.scale)
+    dec = orc.decode(w.k_cache, w.v_cache, one.q, w.block_tables, w.context_lens, w.scale)
+    assert np.array_equal(got1, dec)
+
+
 ALL_PINS = [pin_bruteforce, pin_sdpa, pin_onehot_softmax, pin_constant_v, pin_single_token,
             pin_two_token_closed_form, pin_block_permutation, pin_gqa_repeat, pin_verify_rows,
             pin_zero_length, pin_cache_write, pin_q8_row_closed_form, pin_q8_requant_closed_form,
             pin_q8_zero_and_partial_block, pin_q8_error_bound, pin_q8_lossless_attention,
-            pin_ragged_verify]
+            pin_ragged_verify, pin_prefill_sdpa]
 
 
 if __name__ == "__main__":

@@ -489,22 +489,24 @@ def measure_prefill(device, flush, steps: int = 10) -> dict:
         q, qs = pa.to_torch(rw.q, device), pa.to_torch(rw.query_start, device)
         tb, ln = pa.to_torch(w.block_tables, device), pa.to_torch(w.context_lens, device)
         o = torch.empty_like(q)
-        ts = []
-        for k in range(steps + 3):
-            flush()
-            gpu_hold()
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            e0.record()
-            pa.pa_prefill(kc, vc, q, qs, tb, ln, w.max_context_len, w.scale, rw.max_queries, out=o)
-            e1.record()
-            torch.cuda.synchronize()
-            if k >= 3:
-                ts.append(e0.elapsed_time(e1))
-        us = statistics.mean(ts) * 1e3
         fl = prefill_flops(lens, chunks, hq)
-        out[name] = {"us_per_call": round(us, 2), "gflop": round(fl / 1e9, 2),
-                     "tflops": round(fl / (us * 1e-6) / 1e12, 1), "bound": "tensor",
-                     "frac_of_measured_bf16": round(fl / (us * 1e-6) / 1e12 / peak, 3)}
+        for kernel, suffix in (("tc", ""), ("mma", "_mma")):
+            ts = []
+            for k in range(steps + 3):
+                flush()
+                gpu_hold()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record()
+                pa.pa_prefill(kc, vc, q, qs, tb, ln, w.max_context_len, w.scale, rw.max_queries, out=o,
+                              kernel=kernel)
+                e1.record()
+                torch.cuda.synchronize()
+                if k >= 3:
+                    ts.append(e0.elapsed_time(e1))
+            us = statistics.mean(ts) * 1e3
+            out[name + suffix] = {"kernel": kernel, "us_per_call": round(us, 2), "gflop": round(fl / 1e9, 2),
+                                  "tflops": round(fl / (us * 1e-6) / 1e12, 1), "bound": "tensor",
+                                  "frac_of_measured_bf16": round(fl / (us * 1e-6) / 1e12 / peak, 3)}
     return out
 
 

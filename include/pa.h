@@ -118,14 +118,16 @@ typedef struct pa_cache {
     void *v_scale;
 } pa_cache;
 
-/* Kernel choice for pa_decode / pa_verify. */
+/* Kernel choice for pa_decode / pa_verify / pa_prefill. */
 typedef enum pa_kernel {
     PA_KERNEL_AUTO = 0,    /* bf16: PA_KERNEL_MMA; fp32: PA_KERNEL_SIMT */
     PA_KERNEL_MMA = 1,     /* bf16 only: a producer warp stages 16-token K/V tiles with TMA
                               tensor loads; bf16 tensor-core products, fp32 softmax */
     PA_KERNEL_SIMT = 2,    /* CUDA-core fp32 arithmetic, any dtype (fp32 caches; comparison) */
-    PA_KERNEL_MMA_LDG = 3  /* bf16 only: as PA_KERNEL_MMA but each warp loads its own tiles with
+    PA_KERNEL_MMA_LDG = 3, /* bf16 only: as PA_KERNEL_MMA but each warp loads its own tiles with
                               16-byte loads staged through shared memory (kept for comparison) */
+    PA_KERNEL_TC = 4       /* pa_prefill only (its default): tcgen05 products with the S and O
+                              accumulators and the Q and P operands in tensor memory */
 } pa_kernel;
 
 /* Optional tuning for pa_decode / pa_verify; pass NULL for the defaults. */
@@ -309,6 +311,10 @@ pa_status pa_verify_ragged(const pa_cache *cache, const void *d_q, void *d_out, 
  *                  max_queries bounds every n_b (it sizes the grid).
  *   d_workspace    optional (NULL: no status word): a 256-byte-aligned buffer of
  *                  >= 256 bytes whose first word receives PA_FLAG_* bits.
+ *   opts           optional; only opts->kernel is read: PA_KERNEL_AUTO or
+ *                  PA_KERNEL_TC (tcgen05 kernel, two CTAs per SM) or
+ *                  PA_KERNEL_MMA (warp-level mma.sync kernel, kept for
+ *                  comparison); anything else returns PA_ERR_UNSUPPORTED.
  *   Other arguments as in pa_decode. No split-K: one CTA reads the whole
  *   visible context of its 128 rows.
  */
@@ -316,7 +322,7 @@ pa_status pa_prefill(const pa_cache *cache, const void *d_q, void *d_out, const 
                      int32_t total_queries, int32_t max_queries, const int32_t *d_block_tables,
                      int32_t max_blocks_per_seq, const int32_t *d_context_lens, int32_t batch, int32_t q_heads,
                      int32_t max_context_len, float scale, void *d_workspace, size_t workspace_bytes,
-                     void *stream);
+                     const pa_options *opts, void *stream);
 
 /*
  * pa_validate: check the device-resident per-step inputs without attending.

@@ -25,6 +25,7 @@ PA_KERNEL_AUTO = 0
 PA_KERNEL_MMA = 1
 PA_KERNEL_SIMT = 2
 PA_KERNEL_MMA_LDG = 3
+PA_KERNEL_TC = 4
 PA_DEFAULT_PREFETCH = 1
 PA_DEFAULT_WARPS = 4
 
@@ -103,7 +104,7 @@ def load(path: Path | None = None):
         "pa_verify_ragged": (ctypes.c_int, [cache_p, vp, vp, vp, vp, vp, vp, i32, i32, vp, i32, vp, i32, i32,
                                             i32, ctypes.c_float, vp, ctypes.c_size_t, opts_p, vp]),
         "pa_prefill": (ctypes.c_int, [cache_p, vp, vp, vp, i32, i32, vp, i32, vp, i32, i32, i32,
-                                      ctypes.c_float, vp, ctypes.c_size_t, vp]),
+                                      ctypes.c_float, vp, ctypes.c_size_t, opts_p, vp]),
         "pa_validate": (ctypes.c_int, [cache_p, vp, i32, vp, i32, i32, vp, i32, vp, vp]),
         "pa_decode_noalloc": (ctypes.c_int, [cache_p, vp, vp, vp, i32, vp, i32, i32, i32,
                                              ctypes.c_float, opts_p, vp]),

@@ -18,7 +18,7 @@ from . import _lib as L
 
 _DTYPES = {torch.bfloat16: L.PA_DTYPE_BF16, torch.float32: L.PA_DTYPE_F32, torch.uint8: L.PA_DTYPE_INT8}
 _KERNELS = {"auto": L.PA_KERNEL_AUTO, "mma": L.PA_KERNEL_MMA, "simt": L.PA_KERNEL_SIMT,
-            "mma_ldg": L.PA_KERNEL_MMA_LDG}
+            "mma_ldg": L.PA_KERNEL_MMA_LDG, "tc": L.PA_KERNEL_TC}
 
 
 def _vp(t: Optional[torch.Tensor]):
@@ -239,11 +239,11 @@ def pa_verify_ragged(k_cache, v_cache, q, k_new, v_new, slot_mapping, query_star
 
 
 def pa_prefill(k_cache, v_cache, q, query_start, block_tables, context_lens, max_context_len: int,
-               scale: float, max_queries: int, out=None, workspace=None, stream=None):
+               scale: float, max_queries: int, out=None, workspace=None, stream=None, kernel: str = "auto"):
     """Causal attention of each sequence's prompt chunk (its last n_b positions,
     already in the cache) over its paged context. q: [total, q_heads, head_dim]
     bf16; query_start: int32 [batch + 1]. workspace (optional) receives the
-    status word."""
+    status word. kernel: "auto" / "tc" (tcgen05) or "mma" (warp-level)."""
     cache = make_cache(k_cache, v_cache)
     _need(q.dim() == 3 and q.dtype == k_cache.dtype and q.is_contiguous(),
           "q must be [total_queries, q_heads, head_dim] of the cache dtype")
@@ -258,7 +258,7 @@ def pa_prefill(k_cache, v_cache, q, query_start, block_tables, context_lens, max
     L.check("pa_prefill", L.load().pa_prefill(
         ctypes.byref(cache), _vp(q), _vp(out), _vp(query_start), total, int(max_queries), _vp(block_tables),
         mbps, _vp(context_lens), batch, q_heads, int(max_context_len), float(scale), _vp(workspace), ws_bytes,
-        _stream(stream)))
+        ctypes.byref(_options(0, kernel)), _stream(stream)))
     return out
 
 

@@ -25,6 +25,8 @@ cudaError_t launch_cache_write_q8(const pa_cache* c, const void* k_new, const vo
                                   const int32_t* slots, int32_t n, uint32_t* status, cudaStream_t stream);
 cudaError_t launch_attn_prefill(const CUtensorMap& tk, const CUtensorMap& tv, const AttnParams& p, dim3 grid,
                                 cudaStream_t stream);
+cudaError_t launch_attn_prefill_tc(const CUtensorMap& tk, const CUtensorMap& tv, const AttnParams& p, dim3 grid,
+                                   cudaStream_t stream);
 constexpr int kPrefillRows = 128;  // query rows per prefill CTA
 }  // namespace pa
 
@@ -473,10 +475,12 @@ pa_status pa_prefill(const pa_cache* cache, const void* q, void* out, const int3
                      int32_t total_queries, int32_t max_queries, const int32_t* block_tables,
                      int32_t max_blocks_per_seq, const int32_t* context_lens, int32_t batch, int32_t q_heads,
                      int32_t max_context_len, float scale, void* workspace, size_t workspace_bytes,
-                     void* stream) {
+                     const pa_options* opts, void* stream) {
   pa_status st = check_cache(cache);
   if (st != PA_OK) return st;
   if (cache->dtype != PA_DTYPE_BF16) return PA_ERR_UNSUPPORTED;
+  const int32_t kernel = opts ? opts->kernel : PA_KERNEL_AUTO;
+  if (kernel != PA_KERNEL_AUTO && kernel != PA_KERNEL_TC && kernel != PA_KERNEL_MMA) return PA_ERR_UNSUPPORTED;
   if (batch < 0 || total_queries < 0 || max_queries < 1 || max_context_len < 0 || q_heads <= 0)
     return PA_ERR_INVALID_ARG;
   if (q_heads % cache->kv_heads || !std::isfinite(scale)) return PA_ERR_INVALID_ARG;
@@ -521,7 +525,9 @@ pa_status pa_prefill(const pa_cache* cache, const void* q, void* out, const int3
       !make_pool_map(&tv, cache->v, cache->kv_heads, cache->num_blocks))
     return cuda_fail(cudaErrorInvalidValue);
   const dim3 grid(unsigned(tiles), unsigned(cache->kv_heads), unsigned(batch));
-  const cudaError_t e = launch_attn_prefill(tk, tv, p, grid, static_cast<cudaStream_t>(stream));
+  const cudaError_t e = kernel == PA_KERNEL_MMA
+                            ? launch_attn_prefill(tk, tv, p, grid, static_cast<cudaStream_t>(stream))
+                            : launch_attn_prefill_tc(tk, tv, p, grid, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? PA_OK : cuda_fail(e);
 }
 

@@ -129,3 +129,25 @@ def test_int8_pool_arguments(lib):
         assert _decode(lib, _cache(**ok), opts=_lib.PaOptions(0, kernel)) == _lib.PA_ERR_UNSUPPORTED
     assert lib.pa_cache_write(ctypes.byref(_cache(**{**ok, "k_scale": None})), 0x80000, 0x90000, 0xa0000, 4,
                               None) == _lib.PA_ERR_INVALID_ARG
+
+
+def _prefill(lib, cache, opts=None, batch=2, total=8, max_q=4, hq=12, q=0x30000):
+    return lib.pa_prefill(ctypes.byref(cache), q, 0x40000, 0x80000, total, max_q, 0x50000, 4, 0x60000, batch, hq,
+                          64, ctypes.c_float(0.1), None, 0, ctypes.byref(opts) if opts is not None else None, None)
+
+
+def test_prefill_arguments(lib):
+    """pa_prefill runs the tcgen05 kernel (the default) or the warp-level one,
+    bf16 only; the enum value matches the header."""
+    text = HEADER.read_text()
+    assert re.search(r"PA_KERNEL_TC = (\d+)", text).group(1) == str(_lib.PA_KERNEL_TC)
+    c = _cache()
+    for kernel in (_lib.PA_KERNEL_SIMT, _lib.PA_KERNEL_MMA_LDG, 9):
+        assert _prefill(lib, c, _lib.PaOptions(0, kernel)) == _lib.PA_ERR_UNSUPPORTED
+    for kernel in (_lib.PA_KERNEL_AUTO, _lib.PA_KERNEL_TC, _lib.PA_KERNEL_MMA):
+        assert _prefill(lib, c, _lib.PaOptions(0, kernel), batch=0) == _lib.PA_OK
+    assert _prefill(lib, c, batch=0) == _lib.PA_OK
+    assert _prefill(lib, c, hq=13) == _lib.PA_ERR_INVALID_ARG
+    assert _prefill(lib, c, max_q=0) == _lib.PA_ERR_INVALID_ARG
+    assert _prefill(lib, c, q=0x30008) == _lib.PA_ERR_INVALID_ARG
+    assert _prefill(lib, _cache(dtype=_lib.PA_DTYPE_F32)) == _lib.PA_ERR_UNSUPPORTED

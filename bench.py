@@ -68,6 +68,9 @@ def parse_args():
     ap.add_argument("--unfused", action="store_true",
                     help="time a decode step as two calls, pa_cache_write then pa_decode")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="CPU baseline sample budget")
+    ap.add_argument("--prefill", action="store_true",
+                    help="time only the paged prefill workloads (both kernels, --steps calls each) and print "
+                         "their line")
     return ap.parse_args()
 
 
@@ -776,9 +779,22 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+def run_prefill_only(args):
+    """One JSON line with the prefill measurements alone (profiling runs)."""
+    import torch
+
+    device = torch.device("cuda", 0)
+    torch.cuda.set_device(device)
+    res = measure_prefill(device, make_l2_flush(device), steps=max(1, args.steps))
+    print(json.dumps({"metric": "paged prefill throughput", "unit": "TFLOP/s", "steps": args.steps,
+                      "dtype": "bf16", "data": "synthetic", "per_config": res}), flush=True)
+
+
 def main():
     args = parse_args()
-    if args.impl == "reference":
+    if args.prefill:
+        run_prefill_only(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_native(args)

@@ -7,29 +7,31 @@
 // r = i * group + g. Here the products run as single-thread-issued
 // tcgen05.mma with the accumulators in tensor memory:
 //
-//   S (128 rows x 64 positions, fp32)  = Q . K^T   A = Q in tensor memory, B = K tile in shared memory
+//   S (128 rows x 64 positions, fp32)  = Q . K^T   A = Q in shared memory,  B = K tile in shared memory
 //   O (128 rows x 128 dims, fp32)     += P . V     A = P in tensor memory, B = V tile in shared memory
 //
 // Tensor memory (256 columns of 128 lanes, lane = query row): O in columns
-// 0..127, S in 128..191 (overwritten in place by P as bf16 pairs: the high
-// parts in 128..159, the low parts in 160..191), Q in 192..255 as bf16 pairs.
-// P enters the product as hi + lo (hi = bf16(p), lo = bf16(p - hi)), so the
-// weights keep about 16 mantissa bits, as in the warp-level kernels.
+// 0..127, S in 128..191, P in 192..255 as bf16 pairs. P enters the product
+// as hi + lo (hi = bf16(p), lo = bf16(p - hi)), so the weights keep about 16
+// mantissa bits, as in the warp-level kernels: the high parts in columns
+// 192..223, the low parts in 224..255. Q is a K-major 128-byte-swizzled
+// [2 halves][128 rows][64 dims] tile in shared memory.
 //
 // Roles (192 threads): warps 0..3 own one query row per thread (tensor-memory
 // lane = thread): they load Q, run the online softmax on S, write P, rescale
 // O when the running max moves by more than 2^8, and write the output. Warp 4
 // stages K and V tiles of 64 positions (4 blocks, one 3-D TMA box of 16 rows
-// x 64 dims per block and half) through a 3-stage ring. Warp 5 allocates the
+// x 64 dims per block and half) through 2-stage rings. Warp 5 allocates the
 // tensor memory and one of its threads issues the MMAs. Shared memory holds
-// only the ring (96 KiB), so two CTAs share an SM and one's softmax overlaps
-// the other's products.
+// 96 KiB (Q and the rings), so two CTAs share an SM and one's softmax overlaps the other's
+// products.
 //
-// Per 64-position step j: S_j needs K_j and the previous step's P.V done
-// (S shares its columns with P); the softmax waits for S_j, then P.V_j runs
-// on P_j and V_j. Context rows past the end of the last block read as zero
-// weights; their V rows are zeroed in shared memory before the product (a
-// zero weight times a stale V must stay zero).
+// Per 64-position step j: as soon as the softmax has read S_j into registers
+// the next S_{j+1} is issued, so it runs during step j's exponentials; P.V_j
+// runs once P_j is written, during step j + 1's softmax, which waits for it
+// only before it touches O or overwrites P. Context rows past the end of the
+// last block read as zero weights; their V rows are zeroed in shared memory
+// before the product (a zero weight times a stale V must stay zero).
 #include "tc.cuh"
 
 namespace pa {
@@ -37,30 +39,28 @@ namespace pa {
 constexpr int kTcRows = 128;                  // query rows per CTA (tensor-memory lanes)
 constexpr int kTcTile = 64;                   // context positions per step
 constexpr int kTcTileBlocks = kTcTile / kBlockSize;
-constexpr int kTcStages = 3;
+constexpr int kTcStages = 2;
 constexpr int kTcThreads = 192;               // 4 softmax warps, TMA warp, MMA warp
 constexpr int kTcTileBytes = kTcTile * kHeadDim * 2;  // one K or V tile: [2 halves][64 positions][64 dims]
 constexpr int kTcHalf = kTcTileBytes / 2;
 constexpr uint32_t kTcCols = 256;             // tensor-memory columns per CTA
-constexpr uint32_t kColO = 0, kColS = 128, kColQ = 192;
+constexpr uint32_t kColO = 0, kColS = 128, kColP = 192;
 constexpr float kRescaleLog2 = 8.f;           // O is rescaled once the max grows by more than this
+
+constexpr int kTcQBytes = kTcRows * kHeadDim * 2;  // Q: [2 halves][128 rows][64 dims] bf16
 
 struct TcSmem {
   static constexpr int k = 0;
   static constexpr int v = kTcStages * kTcTileBytes;
-  static constexpr int bars = 2 * kTcStages * kTcTileBytes;
-  // k_full[S], k_empty[S], v_full[S], v_empty[S], v_land, q_full, s_full, p_full, o_done, drain
-  static constexpr int nbars = 4 * kTcStages + 6;
+  static constexpr int q = 2 * kTcStages * kTcTileBytes;
+  static constexpr int bars = q + kTcQBytes;
+  // k_full[S], k_empty[S], v_full[S], v_empty[S], v_land, q_full, s_full, s_free, p_full, o_done, drain
+  static constexpr int nbars = 4 * kTcStages + 7;
   static constexpr int tmem_slot = bars + nbars * 8;
   static constexpr int abort_flag = tmem_slot + 4;
   static constexpr int total = abort_flag + 4;
   static constexpr int alloc = total + 1024;
 };
-
-__device__ __forceinline__ void f32x32_from_u32(float (&v)[32], const uint32_t (&u)[32]) {
-#pragma unroll
-  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(u[i]);
-}
 
 __global__ void __launch_bounds__(kTcThreads, 2)
     attn_prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
@@ -76,7 +76,8 @@ __global__ void __launch_bounds__(kTcThreads, 2)
   const uint32_t b_vland = bv_empty + 8 * kTcStages;  // last V tile, before its stale rows are zeroed
   const uint32_t b_qfull = b_vland + 8;
   const uint32_t b_sfull = b_qfull + 8;
-  const uint32_t b_pfull = b_sfull + 8;
+  const uint32_t b_sfree = b_sfull + 8;  // the softmax has read S (S may be overwritten)
+  const uint32_t b_pfull = b_sfree + 8;
   const uint32_t b_odone = b_pfull + 8;
   const uint32_t b_drain = b_odone + 8;
   volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(sbase + TcSmem::tmem_slot);
@@ -121,6 +122,7 @@ __global__ void __launch_bounds__(kTcThreads, 2)
     mbar_init(b_vland, 1);
     mbar_init(b_qfull, kTcRows);
     mbar_init(b_sfull, 1);
+    mbar_init(b_sfree, kTcRows);
     mbar_init(b_pfull, kTcRows);
     mbar_init(b_odone, 1);
     mbar_init(b_drain, 1);
@@ -229,36 +231,54 @@ __global__ void __launch_bounds__(kTcThreads, 2)
     if (lane == 0) {
       const uint32_t id_s = tc_idesc_bf16(kTcRows, kTcTile, false, false);
       const uint32_t id_o = tc_idesc_bf16(kTcRows, kHeadDim, false, true);
-      bool ok = mbar_wait(b_qfull, 0);
-      for (int j = 0; j < ntile && ok; ++j) {
-        const int s = j % kTcStages, par = (j / kTcStages) & 1;
-        if (*abort_flag || !mbar_wait(bk_full + 8 * s, par) || (j > 0 && !mbar_wait(b_odone, (j - 1) & 1))) {
-          ok = false;
-          break;
-        }
-        tc_fence_after_sync();
-        // S = Q . K^T: 8 steps of 16 dims; K is K-major (positions x dims).
-        const uint32_t ks = base + TcSmem::k + s * kTcTileBytes;
+      // Descriptors are built once; a byte offset d within an operand adds
+      // d >> 4 to the descriptor's start-address field.
+      const uint64_t q_desc = tc_smem_desc(base + TcSmem::q, 16, 1024);
+      const uint64_t k_desc = tc_smem_desc(base + TcSmem::k, 16, 1024);
+      const uint64_t v_desc = tc_smem_desc(base + TcSmem::v, kTcHalf, 1024);
+      // S = Q . K^T: 8 steps of 16 dims; Q and K are K-major (rows x dims).
+      auto issue_s = [&](int j) {
+        const int s = j % kTcStages;
+        const uint64_t kd = k_desc + uint64_t((s * kTcTileBytes) >> 4);
 #pragma unroll
-        for (int kk = 0; kk < kHeadDim / 16; ++kk)
-          tc_mma_ts(tmem + kColS, tmem + kColQ + kk * 8,
-                    tc_smem_desc(ks + (kk >> 2) * kTcHalf + (kk & 3) * 32, 16, 1024), id_s, kk > 0);
+        for (int kk = 0; kk < kHeadDim / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * kTcHalf + (kk & 3) * 32;
+          const uint32_t qoff = (kk >> 2) * (kTcQBytes / 2) + (kk & 3) * 32;
+          tc_mma(tmem + kColS, q_desc + (qoff >> 4), kd + (off >> 4), id_s, kk > 0);
+        }
         tc_commit(b_sfull);
         tc_commit(bk_empty + 8 * s);
+      };
+      bool ok = mbar_wait(b_qfull, 0) && mbar_wait(bk_full, 0);
+      if (ok) {
+        tc_fence_after_sync();
+        issue_s(0);
+      }
+      for (int j = 0; j < ntile && ok; ++j) {
+        const int s = j % kTcStages, par = (j / kTcStages) & 1;
+        if (j + 1 < ntile) {
+          const int s1 = (j + 1) % kTcStages, par1 = ((j + 1) / kTcStages) & 1;
+          if (*abort_flag || !mbar_wait(b_sfree, j & 1) || !mbar_wait(bk_full + 8 * s1, par1)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after_sync();
+          issue_s(j + 1);
+        }
         if (!mbar_wait(b_pfull, j & 1) || !mbar_wait(bv_full + 8 * s, par)) {
           ok = false;
           break;
         }
         tc_fence_after_sync();
-        // O += P_hi . V + P_lo . V: 4 steps of 16 positions; V is MN-major
-        // (positions x dims, dims contiguous): 64-dim halves kTcHalf apart,
-        // 8-position groups 1024 bytes apart.
-        const uint32_t vs = base + TcSmem::v + s * kTcTileBytes;
+        // O += P_hi . V + P_lo . V: 4 steps of 16 positions. P (rows x
+        // positions) is in tensor memory; V is MN-major (positions x dims,
+        // dims contiguous): 64-dim halves kTcHalf apart, 8-position groups
+        // 1024 bytes apart.
+        const uint64_t vd = v_desc + uint64_t((s * kTcTileBytes) >> 4);
 #pragma unroll
         for (int kk = 0; kk < kTcTile / 16; ++kk) {
-          const uint64_t vd = tc_smem_desc(vs + kk * 2048, kTcHalf, 1024);
-          tc_mma_ts(tmem + kColO, tmem + kColS + kk * 8, vd, id_o, j > 0 || kk > 0);
-          tc_mma_ts(tmem + kColO, tmem + kColS + 32 + kk * 8, vd, id_o, true);
+          tc_mma_ts(tmem + kColO, tmem + kColP + kk * 8, vd + uint64_t((kk * 2048) >> 4), id_o, j > 0 || kk > 0);
+          tc_mma_ts(tmem + kColO, tmem + kColP + 32 + kk * 8, vd + uint64_t((kk * 2048) >> 4), id_o, true);
         }
         tc_commit(b_odone);
         tc_commit(bv_empty + 8 * s);
@@ -278,24 +298,16 @@ __global__ void __launch_bounds__(kTcThreads, 2)
     const bool live = r < nrows;
     const uint32_t trow = tmem + (uint32_t(warp * 32) << 16);
     {
+      // Row r of Q: 16 chunks of 8 dims, 128-byte swizzle (chunk ^ (r & 7)) in each 64-dim half.
       const uint4* qrow = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.q) +
                                                          row_offset(p, q0, h, row0 + (live ? r : 0)));
+      uint8_t* qs = sbase + TcSmem::q + r * 128;
 #pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        uint32_t u[32];
-#pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          const uint4 x = live ? __ldg(qrow + half * 8 + c) : make_uint4(0, 0, 0, 0);
-          u[4 * c] = x.x;
-          u[4 * c + 1] = x.y;
-          u[4 * c + 2] = x.z;
-          u[4 * c + 3] = x.w;
-        }
-        float v[32];
-        f32x32_from_u32(v, u);
-        tc_st32(trow + kColQ + half * 32, v);
+      for (int c = 0; c < kHeadDim / 8; ++c) {
+        const uint4 x = live ? __ldg(qrow + c) : make_uint4(0, 0, 0, 0);
+        *reinterpret_cast<uint4*>(qs + (c >> 3) * (kTcQBytes / 2) + (((c & 7) ^ (r & 7)) << 4)) = x;
       }
-      tc_fence_before_sync();
+      fence_proxy_async_smem();
       mbar_arrive(b_qfull);
     }
     const int lim = live ? row_limit(p, L, nq, row0 + r) : -1;
@@ -307,45 +319,64 @@ __global__ void __launch_bounds__(kTcThreads, 2)
         break;
       }
       tc_fence_after_sync();
+      uint32_t sr[kTcTile / 2], sr2[kTcTile / 2];
+      tc_ld32_issue(trow + kColS, sr);
+      tc_ld32_issue(trow + kColS + 32, sr2);
+      tc_wait_ld(sr);
+      tc_wait_ld(sr2);
+      tc_fence_before_sync();
+      mbar_arrive(b_sfree);
       float s[kTcTile];
-      {
-        float a[32], c[32];
-        tc_ld32(trow + kColS, a);
-        tc_ld32(trow + kColS + 32, c);
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          s[i] = a[i];
-          s[32 + i] = c[i];
-        }
+      for (int i = 0; i < kTcTile / 2; ++i) {
+        s[i] = __uint_as_float(sr[i]);
+        s[kTcTile / 2 + i] = __uint_as_float(sr2[i]);
       }
-      // Scale to base-2 units, mask past the row's limit, take the tile max.
+      // Tile max in base-2 units. A tile wholly inside the row's limit takes
+      // the max of the raw scores (scale >= 0) and folds the scale into the
+      // exponent's FMA; otherwise the scores are scaled and masked here.
       const int t0 = j * kTcTile;
-      float mx = -INFINITY;
-      if (t0 + kTcTile - 1 <= lim) {
+      const bool whole = t0 + kTcTile - 1 <= lim && p.scale_log2 >= 0.f;
+      float mk[8];
 #pragma unroll
-        for (int i = 0; i < kTcTile; ++i) {
-          s[i] *= p.scale_log2;
-          mx = fmaxf(mx, s[i]);
-        }
+      for (int k = 0; k < 8; ++k) mk[k] = -INFINITY;
+      if (whole) {
+#pragma unroll
+        for (int i = 0; i < kTcTile; ++i) mk[i & 7] = fmaxf(mk[i & 7], s[i]);
       } else {
 #pragma unroll
         for (int i = 0; i < kTcTile; ++i) {
           s[i] = t0 + i <= lim ? s[i] * p.scale_log2 : -INFINITY;
-          mx = fmaxf(mx, s[i]);
+          mk[i & 7] = fmaxf(mk[i & 7], s[i]);
         }
       }
+      float mx = fmaxf(fmaxf(fmaxf(mk[0], mk[1]), fmaxf(mk[2], mk[3])), fmaxf(fmaxf(mk[4], mk[5]), fmaxf(mk[6], mk[7])));
+      const float mul = whole ? p.scale_log2 : 1.f;
+      if (whole) mx *= mul;
       // Online softmax with a lazy reference max: m moves (and O, l are
       // rescaled) only when the tile max exceeds it by more than 2^8, so
       // weights stay <= 256.
       const float m_new = fmaxf(m, mx);
       const bool move = m_new > m + kRescaleLog2;
+      // P.V of the previous step must be done before O is touched or P
+      // rewritten: waited for here only when O needs rescaling, else after
+      // the exponentials.
+      bool pv_done = j == 0;
       if (__any_sync(0xffffffffu, move)) {
+        if (!pv_done) {
+          if (!__all_sync(0xffffffffu, mbar_wait(b_odone, (j - 1) & 1))) {
+            ok = false;
+            break;
+          }
+          tc_fence_after_sync();
+          pv_done = true;
+        }
         const float alpha = move ? fast_exp2(m - m_new) : 1.f;
         if (move) {
           l *= alpha;
           m = m_new;
         }
-        if (j > 0) {  // P.V of the previous step is complete (S_j was issued after it)
+        if (j > 0) {
 #pragma unroll 1
           for (int c = 0; c < kHeadDim / 32; ++c) {
             float o[32];
@@ -356,20 +387,42 @@ __global__ void __launch_bounds__(kTcThreads, 2)
           }
         }
       }
+      // p = 2^(s * mul - m), summed in 8 partial sums; P = hi + lo as bf16 pairs.
       const float m_use = m == -INFINITY ? 0.f : m;
-      float hi[32], lo[32], ps0 = 0.f, ps1 = 0.f;
+      const uint64_t mul2 = f2_pack(mul, mul), neg2 = f2_pack(-m_use, -m_use);
+      uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
+      uint32_t hi[32], lo[32];
 #pragma unroll
       for (int c = 0; c < 32; ++c) {
-        const float p0 = fast_exp2(s[2 * c] - m_use), p1 = fast_exp2(s[2 * c + 1] - m_use);
-        ps0 += p0;
-        ps1 += p1;
+        float a0, a1;
+        f2_unpack(f2_fma(f2_pack(s[2 * c], s[2 * c + 1]), mul2, neg2), a0, a1);
+        const float p0 = fast_exp2(a0), p1 = fast_exp2(a1);
+        const uint64_t pp = f2_pack(p0, p1);
+        acc[c & 3] = f2_add(acc[c & 3], pp);
         const uint32_t x = pack_bf16x2(p0, p1);
-        hi[c] = __uint_as_float(x);
-        lo[c] = __uint_as_float(pack_bf16x2(p0 - bf16_lo(x), p1 - bf16_hi(x)));
+        hi[c] = x;
+        float r0, r1;
+        f2_unpack(f2_sub(pp, f2_pack(bf16_lo(x), bf16_hi(x))), r0, r1);
+        lo[c] = pack_bf16x2(r0, r1);
       }
-      l += ps0 + ps1;
-      tc_st32(trow + kColS, hi);
-      tc_st32(trow + kColS + 32, lo);
+      float sum = 0.f;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        float a0, a1;
+        f2_unpack(acc[k], a0, a1);
+        sum += a0 + a1;
+      }
+      l += sum;
+      if (!pv_done) {
+        if (!__all_sync(0xffffffffu, mbar_wait(b_odone, (j - 1) & 1))) {
+          ok = false;
+          break;
+        }
+        tc_fence_after_sync();
+      }
+      tc_st32_issue(trow + kColP, hi);
+      tc_st32_issue(trow + kColP + 32, lo);
+      tc_wait_st();
       tc_fence_before_sync();
       mbar_arrive(b_pfull);
     }

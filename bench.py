@@ -68,6 +68,9 @@ def parse_args():
     ap.add_argument("--unfused", action="store_true",
                     help="time a decode step as two calls, pa_cache_write then pa_decode")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="CPU baseline sample budget")
+    ap.add_argument("--record-traffic", nargs=2, metavar=("WORKLOAD", "NCU_CSV"),
+                    help="store the DRAM bytes of an ncu capture (`ncu -i REPORT --page raw --csv` output) "
+                         "for WORKLOAD (c4, c3, c5, c4_int8, ...) in profiles/decode_traffic.json; no GPU")
     ap.add_argument("--prefill", action="store_true",
                     help="time only the paged prefill workloads (both kernels, --steps calls each) and print "
                          "their line")
@@ -190,13 +193,64 @@ class ClockSampler:
                 "reasons": sorted(reasons)}
 
 
-def kernel_source_hash() -> str:
+# Device sources each timed kernel is built from (with include/pa.h): a
+# recorded traffic figure stays valid while these files are unchanged.
+TRAFFIC_SOURCES = {
+    "attn_mma": ("attn_mma.cu", "mma_tile.cuh", "pa_device.cuh"),
+    "attn_q8": ("attn_q8.cu", "q8.cuh", "mma_tile.cuh", "pa_device.cuh"),
+}
+
+
+def traffic_kernel(workload: str) -> str:
+    return "attn_q8" if workload.endswith("_int8") else "attn_mma"
+
+
+def kernel_source_hash(kernel: str = "attn_mma") -> str:
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "paged_kv_decode_pa_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
-        if name.endswith((".cu", ".cuh")):
-            h.update(open(os.path.join(csrc, name), "rb").read())
+    for name in TRAFFIC_SOURCES[kernel]:
+        h.update(open(os.path.join(csrc, name), "rb").read())
+    h.update(open(os.path.join(ROOT, "include", "pa.h"), "rb").read())
     return h.hexdigest()[:16]
+
+
+def record_traffic(workload: str, csv_path: str) -> dict:
+    """Store one ncu capture's DRAM bytes for a workload in
+    profiles/decode_traffic.json. csv_path: `ncu -i <report> --page raw --csv`
+    output holding one launch of the workload's attention kernel."""
+    import csv
+
+    rows = list(csv.reader(open(csv_path)))
+    hdr = rows[0]
+    data = [r for r in rows[2:] if len(r) == len(hdr)]
+    if len(data) != 1:
+        raise SystemExit(f"{csv_path}: expected one captured launch, found {len(data)}")
+    rec = dict(zip(hdr, data[0]))
+    units = dict(zip(hdr, rows[1]))
+    scale = {"byte": 1, "Kbyte": 1e3, "Mbyte": 1e6, "Gbyte": 1e9}
+
+    def nbytes(name):
+        return int(round(float(rec[name].replace(",", "")) * scale[units[name]]))
+
+    tscale = {"ns": 1e-3, "nsecond": 1e-3, "us": 1.0, "usecond": 1.0, "ms": 1e3, "msecond": 1e3}
+    dur_us = float(rec["gpu__time_duration.sum"].replace(",", "")) * tscale[units["gpu__time_duration.sum"]]
+    kernel = traffic_kernel(workload)
+    if kernel not in rec.get("Kernel Name", ""):
+        raise SystemExit(f"{csv_path}: captured {rec.get('Kernel Name')!r}, expected {kernel}")
+    rd, wr = nbytes("dram__bytes_read.sum"), nbytes("dram__bytes_write.sum")
+    entry = {"kernel": rec.get("Kernel Name"), "kernel_source_hash": kernel_source_hash(kernel),
+             "dram_bytes_per_launch": rd + wr, "dram_read_bytes": rd, "dram_write_bytes": wr,
+             "ncu_duration_us": round(dur_us, 3)}
+    path = os.path.join(ROOT, "profiles", "decode_traffic.json")
+    try:
+        allrec = json.load(open(path))
+    except Exception:
+        allrec = {}
+    allrec[workload] = entry
+    with open(path, "w") as f:
+        json.dump(allrec, f, indent=1)
+        f.write("\n")
+    return entry
 
 
 def ncu_traffic(workload: str):
@@ -207,7 +261,7 @@ def ncu_traffic(workload: str):
     except Exception:
         return None
     entry = rec.get(workload)
-    if not entry or entry.get("kernel_source_hash") != kernel_source_hash():
+    if not entry or entry.get("kernel_source_hash") != kernel_source_hash(traffic_kernel(workload)):
         return None
     return entry.get("dram_bytes_per_launch")
 
@@ -792,7 +846,9 @@ def run_prefill_only(args):
 
 def main():
     args = parse_args()
-    if args.prefill:
+    if args.record_traffic:
+        print(json.dumps(record_traffic(*args.record_traffic)))
+    elif args.prefill:
         run_prefill_only(args)
     elif args.impl == "reference":
         run_reference(args)

@@ -68,3 +68,78 @@ def test_prefill_zero_chunks_and_long_context(kernel):
                       num_queries=256)
     got, ref = _prefill(w, [0, 256, 3], kernel)
     assert_close(got, ref, "bf16", f"prefill long ({kernel})")
+
+
+def _prefill_raw(w, rw, tables, lens, kernel):
+    import torch
+
+    import paged_kv_decode_pa_gb300 as pa
+
+    dev = torch.device("cuda")
+    kc, vc = pa.to_torch(w.k_cache, dev), pa.to_torch(w.v_cache, dev)
+    ws = torch.zeros(256, dtype=torch.uint8, device=dev)
+    out = pa.pa_prefill(kc, vc, pa.to_torch(rw.q, dev), pa.to_torch(rw.query_start, dev), pa.to_torch(tables, dev),
+                        pa.to_torch(lens, dev), w.max_context_len, w.scale, rw.max_queries, workspace=ws,
+                        kernel=kernel)
+    torch.cuda.synchronize()
+    return pa.to_numpy(out), pa.pa_workspace_status(ws)
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_prefill_flags_bad_ids_and_lengths(kernel):
+    """A block id outside the pool raises PA_FLAG_BAD_BLOCK and reads zeros; a
+    length past max_context_len raises PA_FLAG_BAD_LENGTH and is clamped.
+    Neither faults, and the other sequences' rows are unchanged."""
+    from paged_kv_decode_pa_gb300 import _lib
+
+    w = inputs.custom(batch=3, q_heads=12, kv_heads=2, context_lens=(40, 40, 40), num_blocks=16, seed=44,
+                      num_queries=8)
+    rw = inputs.ragged(w, [8, 8, 8])
+    good, st = _prefill_raw(w, rw, w.block_tables, w.context_lens, kernel)
+    assert st == 0
+    tables = w.block_tables.copy()
+    tables[1, 1] = 1 << 30
+    bad, st = _prefill_raw(w, rw, tables, w.context_lens, kernel)
+    assert st & _lib.PA_FLAG_BAD_BLOCK
+    assert np.array_equal(bad[np.r_[0:8, 16:24]], good[np.r_[0:8, 16:24]])
+    lens = w.context_lens.copy()
+    lens[2] = w.max_context_len + 100
+    bad, st = _prefill_raw(w, rw, w.block_tables, lens, kernel)
+    assert st & _lib.PA_FLAG_BAD_LENGTH
+    assert np.array_equal(bad[0:16], good[0:16])
+
+
+def test_prefill_graph_replay():
+    """pa_prefill captured in a CUDA graph: rewrite q and the lengths in place,
+    replay, and match the oracle for the new inputs."""
+    import torch
+
+    import paged_kv_decode_pa_gb300 as pa
+
+    dev = torch.device("cuda")
+    w = inputs.custom(batch=4, q_heads=16, kv_heads=8, context_lens=(300, 200, 64, 129), num_blocks=80, seed=45,
+                      num_queries=64)
+    chunks = [64, 33, 1, 40]
+    rw = inputs.ragged(w, chunks)
+    kc, vc = pa.to_torch(w.k_cache, dev), pa.to_torch(w.v_cache, dev)
+    q, qs = pa.to_torch(rw.q, dev), pa.to_torch(rw.query_start, dev)
+    tb, ln = pa.to_torch(w.block_tables, dev), pa.to_torch(w.context_lens, dev)
+    out = torch.empty_like(q)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        pa.pa_prefill(kc, vc, q, qs, tb, ln, w.max_context_len, w.scale, rw.max_queries, out=out)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        pa.pa_prefill(kc, vc, q, qs, tb, ln, w.max_context_len, w.scale, rw.max_queries, out=out)
+    rng = np.random.default_rng(46)
+    q2 = rng.standard_normal(rw.q.shape).astype(np.float32)
+    q2 = pa.to_numpy(torch.from_numpy(q2).to(torch.bfloat16))
+    lens2 = w.context_lens.copy()
+    lens2[0] -= 5  # the chunk now ends 5 positions earlier
+    q.copy_(pa.to_torch(q2, dev))
+    ln.copy_(pa.to_torch(lens2, dev))
+    g.replay()
+    torch.cuda.synchronize()
+    ref = oracle.attend_ragged(w.k_cache, w.v_cache, q2, rw.query_start, w.block_tables, lens2, w.scale)
+    assert_close(to_f64(pa.to_numpy(out)), ref, "bf16", "prefill graph replay")

@@ -2,14 +2,19 @@
  * pa.h: C ABI of libpa, decode-time attention over a paged KV cache on one
  * NVIDIA GB300 (sm_103a).
  *
- * Three operations, all asynchronous on the caller's CUDA stream:
+ * Operations, all asynchronous on the caller's CUDA stream:
  *
- *   pa_cache_write  slot-mapping scatter of new K/V rows into the block pool;
- *   pa_decode       grouped-query attention of one query token per sequence
- *                   over that sequence's cached context, read in place
- *                   through its block table;
- *   pa_verify       the k+1-token speculative-verify variant: writes the new
- *                   tokens' K/V and attends with a causal mask among them.
+ *   pa_cache_write    slot-mapping scatter of new K/V rows into the block pool;
+ *   pa_decode         grouped-query attention of one query token per sequence
+ *                     over that sequence's cached context, read in place
+ *                     through its block table;
+ *   pa_verify         the k+1-token speculative-verify variant: writes the new
+ *                     tokens' K/V and attends with a causal mask among them;
+ *   pa_verify_ragged  the same with a different number of new tokens per
+ *                     sequence (query_start), decode rows included;
+ *   pa_prefill        causal attention of prompt chunks already in the cache;
+ *   pa_validate       a device-side check of tables, lengths and slots;
+ *   pa_decode_noalloc pa_decode with library-owned scratch.
  *
  * Where each operation is defined:
  *  - The cache is head-major, [kv_heads, num_blocks, block_size, head_dim], so

@@ -205,12 +205,21 @@ def traffic_kernel(workload: str) -> str:
     return "attn_q8" if workload.endswith("_int8") else "attn_mma"
 
 
+def header_code(text: str) -> str:
+    """include/pa.h without its comments and blank space: what a kernel sees."""
+    import re
+
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    return " ".join(text.split())
+
+
 def kernel_source_hash(kernel: str = "attn_mma") -> str:
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "paged_kv_decode_pa_gb300", "csrc")
     for name in TRAFFIC_SOURCES[kernel]:
         h.update(open(os.path.join(csrc, name), "rb").read())
-    h.update(open(os.path.join(ROOT, "include", "pa.h"), "rb").read())
+    h.update(header_code(open(os.path.join(ROOT, "include", "pa.h")).read()).encode())
     return h.hexdigest()[:16]
 
 

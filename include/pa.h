@@ -317,9 +317,11 @@ pa_status pa_verify_ragged(const pa_cache *cache, const void *d_q, void *d_out, 
  *   d_workspace    optional (NULL: no status word): a 256-byte-aligned buffer of
  *                  >= 256 bytes whose first word receives PA_FLAG_* bits.
  *   opts           optional; only opts->kernel is read: PA_KERNEL_AUTO or
- *                  PA_KERNEL_TC (tcgen05 kernel, two CTAs per SM) or
+ *                  PA_KERNEL_TC (tcgen05 kernel, two CTAs per SM; needs
+ *                  q_heads / kv_heads <= 128, else PA_ERR_UNSUPPORTED) or
  *                  PA_KERNEL_MMA (warp-level mma.sync kernel, kept for
  *                  comparison); anything else returns PA_ERR_UNSUPPORTED.
+ *                  AUTO takes the tcgen05 kernel when the group allows it.
  *   Other arguments as in pa_decode. No split-K: one CTA reads the whole
  *   visible context of its 128 rows.
  */

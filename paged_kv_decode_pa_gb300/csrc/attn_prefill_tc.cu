@@ -3,8 +3,9 @@
 // Same operation as attn_prefill.cu (causal attention of a prompt chunk over
 // the sequence's paged cache: "From 183 ms to 19 ms per decode step", section
 // "What's next"; the masked softmax of "Anatomy of a Decode-Step Stall",
-// Model._layer), for 128 query rows of one (sequence, KV head) per CTA, rows
-// r = i * group + g. Here the products run as single-thread-issued
+// Model._layer), for the rows r = i * group + g of floor(128 / group) query
+// tokens of one (sequence, KV head) per CTA (rows_per_cta <= 128; the MMA's
+// spare rows are zero). Here the products run as single-thread-issued
 // tcgen05.mma with the accumulators in tensor memory:
 //
 //   S (128 rows x 64 positions, fp32)  = Q . K^T   A = Q in shared memory,  B = K tile in shared memory
@@ -15,13 +16,14 @@
 // as hi + lo (hi = bf16(p), lo = bf16(p - hi)), so the weights keep about 16
 // mantissa bits, as in the warp-level kernels: the high parts in columns
 // 192..223, the low parts in 224..255. Q is a K-major 128-byte-swizzled
-// [2 halves][128 rows][64 dims] tile in shared memory.
+// [2 halves][128 rows][64 dims] tile in shared memory, loaded by two TMA
+// boxes of 64 dims x group heads x tokens, whose rows land in r order.
 //
 // Roles (192 threads): warps 0..3 own one query row per thread (tensor-memory
-// lane = thread): they load Q, run the online softmax on S, write P, rescale
-// O when the running max moves by more than 2^8, and write the output. Warp 4
-// stages K and V tiles of 64 positions (4 blocks, one 3-D TMA box of 16 rows
-// x 64 dims per block and half) through 2-stage rings. Warp 5 allocates the
+// lane = thread): they run the online softmax on S, write P, rescale O when
+// the running max moves by more than 2^8, and write the output. Warp 4 loads
+// Q and stages K and V tiles of 64 positions (4 blocks, one 3-D TMA box of 16
+// rows x 64 dims per block and half) through 2-stage rings. Warp 5 allocates the
 // tensor memory and one of its threads issues the MMAs. Shared memory holds
 // 96 KiB (Q and the rings), so two CTAs share an SM and one's softmax overlaps the other's
 // products.
@@ -64,7 +66,7 @@ struct TcSmem {
 
 __global__ void __launch_bounds__(kTcThreads, 2)
     attn_prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
-                           const AttnParams p) {
+                           const __grid_constant__ CUtensorMap tmap_q, const AttnParams p) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -85,32 +87,11 @@ __global__ void __launch_bounds__(kTcThreads, 2)
 
   const int b = blockIdx.z, h = blockIdx.y;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  int q0, nq;
-  seq_queries(p, b, blockIdx.x == 0 && h == 0, &q0, &nq);
-  int L = __ldg(p.context_lens + b);
-  const int cap = min(p.max_context_len, p.mbps * kBlockSize);
-  if (L < 0 || L > cap) {
-    if (blockIdx.x == 0 && h == 0 && threadIdx.x == 0) raise_flag(p.status, PA_FLAG_BAD_LENGTH);
-    L = L < 0 ? 0 : cap;
-  }
-  const int rows_b = nq * p.group;
-  const int row0 = blockIdx.x * kTcRows;
-  if (row0 >= rows_b) return;
-  const int nrows = min(kTcRows, rows_b - row0);
-  // Positions the CTA's last row may see; every earlier row sees fewer.
-  const int kv_end = max(0, min(L, L - nq + (row0 + nrows - 1) / p.group + 1));
-  const int nblk = (kv_end + kBlockSize - 1) / kBlockSize;
-  const int ntile = (nblk + kTcTileBlocks - 1) / kTcTileBlocks;
-  const int tail_valid = kv_end - (nblk - 1) * kBlockSize;  // rows of the last block inside kv_end
-
-  if (ntile == 0) {  // every row sits at a negative position: zeros
-    if (threadIdx.x < nrows) {
-      uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.out) + row_offset(p, q0, h, row0 + threadIdx.x));
-#pragma unroll
-      for (int c = 0; c < kHeadDim / 8; ++c) dst[c] = make_uint4(0, 0, 0, 0);
-    }
-    return;
-  }
+  const int rpt = p.rows_per_cta;  // rows of this tile: a multiple of the group, at most 128
+  // The sequence's query range and length are loaded first; the barrier
+  // setup and the tensor-memory allocation below overlap their latency.
+  const int qs_a = __ldg(p.query_start + b), qs_e = __ldg(p.query_start + b + 1);
+  const int L_raw = __ldg(p.context_lens + b);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kTcStages; ++s) {
@@ -120,7 +101,7 @@ __global__ void __launch_bounds__(kTcThreads, 2)
       mbar_init(bv_empty + 8 * s, 1);
     }
     mbar_init(b_vland, 1);
-    mbar_init(b_qfull, kTcRows);
+    mbar_init(b_qfull, 1 + (kTcRows - rpt));  // the Q loads, and the threads that zero the spare rows
     mbar_init(b_sfull, 1);
     mbar_init(b_sfree, kTcRows);
     mbar_init(b_pfull, kTcRows);
@@ -138,9 +119,40 @@ __global__ void __launch_bounds__(kTcThreads, 2)
   tc_fence_after_sync();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == 4) {
+  int q0, nq;
+  query_range(p, qs_a, qs_e, blockIdx.x == 0 && h == 0, &q0, &nq);
+  int L = L_raw;
+  const int cap = min(p.max_context_len, p.mbps * kBlockSize);
+  if (L < 0 || L > cap) {
+    if (blockIdx.x == 0 && h == 0 && threadIdx.x == 0) raise_flag(p.status, PA_FLAG_BAD_LENGTH);
+    L = L < 0 ? 0 : cap;
+  }
+  const int rows_b = nq * p.group;
+  const int row0 = blockIdx.x * rpt;
+  const int nrows = max(0, min(rpt, rows_b - row0));
+  // Positions the CTA's last row may see; every earlier row sees fewer.
+  const int kv_end = nrows > 0 ? max(0, min(L, L - nq + (row0 + nrows - 1) / p.group + 1)) : 0;
+  const int nblk = (kv_end + kBlockSize - 1) / kBlockSize;
+  const int ntile = (nblk + kTcTileBlocks - 1) / kTcTileBlocks;
+  const int tail_valid = kv_end - (nblk - 1) * kBlockSize;  // rows of the last block inside kv_end
+
+  if (ntile == 0) {
+    // No rows here, or every row sits at a negative position (zeros).
+    if (threadIdx.x < nrows) {
+      uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.out) + row_offset(p, q0, h, row0 + threadIdx.x));
+#pragma unroll
+      for (int c = 0; c < kHeadDim / 8; ++c) dst[c] = make_uint4(0, 0, 0, 0);
+    }
+  } else if (warp == 4) {
     // ---------------- TMA producer ----------------
     if (lane == 0) {
+      // Q rows row0 .. row0 + rpt - 1: tokens q0 + row0 / group onwards, the
+      // group's heads, one box per 64-dim half.
+      const uint64_t once = policy_evict_first();
+      const int tq = rpt / p.group;
+      mbar_arrive_expect_tx(b_qfull, 2 * rpt * 128);
+      tma_load_3d(base + TcSmem::q, &tmap_q, 0, h * p.group, q0 + blockIdx.x * tq, b_qfull, once);
+      tma_load_3d(base + TcSmem::q + kTcQBytes / 2, &tmap_q, 64, h * p.group, q0 + blockIdx.x * tq, b_qfull, once);
       prefetch_tensormap(&tmap_k);
       prefetch_tensormap(&tmap_v);
     }
@@ -297,16 +309,12 @@ __global__ void __launch_bounds__(kTcThreads, 2)
     const int r = threadIdx.x;
     const bool live = r < nrows;
     const uint32_t trow = tmem + (uint32_t(warp * 32) << 16);
-    {
-      // Row r of Q: 16 chunks of 8 dims, 128-byte swizzle (chunk ^ (r & 7)) in each 64-dim half.
-      const uint4* qrow = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.q) +
-                                                         row_offset(p, q0, h, row0 + (live ? r : 0)));
+    if (r >= rpt) {
+      // A spare MMA row past the tile: zero Q so that its scores are finite.
       uint8_t* qs = sbase + TcSmem::q + r * 128;
 #pragma unroll
-      for (int c = 0; c < kHeadDim / 8; ++c) {
-        const uint4 x = live ? __ldg(qrow + c) : make_uint4(0, 0, 0, 0);
-        *reinterpret_cast<uint4*>(qs + (c >> 3) * (kTcQBytes / 2) + (((c & 7) ^ (r & 7)) << 4)) = x;
-      }
+      for (int c = 0; c < kHeadDim / 8; ++c)
+        *reinterpret_cast<uint4*>(qs + (c >> 3) * (kTcQBytes / 2) + ((c & 7) << 4)) = make_uint4(0, 0, 0, 0);
       fence_proxy_async_smem();
       mbar_arrive(b_qfull);
     }
@@ -457,8 +465,8 @@ __global__ void __launch_bounds__(kTcThreads, 2)
   }
 }
 
-cudaError_t launch_attn_prefill_tc(const CUtensorMap& tk, const CUtensorMap& tv, const AttnParams& p, dim3 grid,
-                                   cudaStream_t stream) {
+cudaError_t launch_attn_prefill_tc(const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tq,
+                                   const AttnParams& p, dim3 grid, cudaStream_t stream) {
   static int configured[64] = {0};
   int dev = 0;
   cudaGetDevice(&dev);
@@ -468,7 +476,7 @@ cudaError_t launch_attn_prefill_tc(const CUtensorMap& tk, const CUtensorMap& tv,
     if (e != cudaSuccess) return e;
     configured[dev] = 1;
   }
-  attn_prefill_tc_kernel<<<grid, kTcThreads, TcSmem::alloc, stream>>>(tk, tv, p);
+  attn_prefill_tc_kernel<<<grid, kTcThreads, TcSmem::alloc, stream>>>(tk, tv, tq, p);
   return cudaGetLastError();
 }
 

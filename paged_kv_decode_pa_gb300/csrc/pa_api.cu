@@ -25,8 +25,8 @@ cudaError_t launch_cache_write_q8(const pa_cache* c, const void* k_new, const vo
                                   const int32_t* slots, int32_t n, uint32_t* status, cudaStream_t stream);
 cudaError_t launch_attn_prefill(const CUtensorMap& tk, const CUtensorMap& tv, const AttnParams& p, dim3 grid,
                                 cudaStream_t stream);
-cudaError_t launch_attn_prefill_tc(const CUtensorMap& tk, const CUtensorMap& tv, const AttnParams& p, dim3 grid,
-                                   cudaStream_t stream);
+cudaError_t launch_attn_prefill_tc(const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tq,
+                                   const AttnParams& p, dim3 grid, cudaStream_t stream);
 constexpr int kPrefillRows = 128;  // query rows per prefill CTA
 }  // namespace pa
 
@@ -140,6 +140,23 @@ bool make_pool_map(CUtensorMap* map, void* pool, int32_t kv_heads, int32_t num_b
   return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, pool, dims, strides, box, estr,
              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Query rows of a prefill, [total][q_heads][128] bf16, in boxes of 64 dims x
+// `group` heads x `tokens` tokens (128-byte swizzle): a box lands as the rows
+// r = token * group + head of one KV head's group. Outside the tensor it
+// reads zeros.
+bool make_query_map(CUtensorMap* map, const void* q, int32_t total, int32_t q_heads, int32_t group,
+                    int32_t tokens) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {cuuint64_t(kHeadDim), cuuint64_t(q_heads), cuuint64_t(total)};
+  cuuint64_t strides[2] = {cuuint64_t(kHeadDim) * 2, cuuint64_t(q_heads) * kHeadDim * 2};
+  cuuint32_t box[3] = {64, cuuint32_t(group), cuuint32_t(tokens)};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(q), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 // The int8 pool's four views: bytes [kv_heads][num_blocks * 16][128] in
@@ -492,8 +509,14 @@ pa_status pa_prefill(const pa_cache* cache, const void* q, void* out, const int3
   if (workspace && ((reinterpret_cast<uintptr_t>(workspace) & 255u) || workspace_bytes < 256))
     return PA_ERR_WORKSPACE;
   if (batch > 65535) return PA_ERR_UNSUPPORTED;
-  const int64_t rows = int64_t(max_queries) * (q_heads / cache->kv_heads);
-  const int64_t tiles = (rows + kPrefillRows - 1) / kPrefillRows;
+  const int32_t group = q_heads / cache->kv_heads;
+  // The tcgen05 kernel takes whole tokens per CTA (floor(128 / group) of
+  // them), so it needs group <= 128; the warp-level kernel takes 128 rows.
+  const bool tc = kernel == PA_KERNEL_TC || (kernel == PA_KERNEL_AUTO && group <= kPrefillRows);
+  if (tc && group > kPrefillRows) return PA_ERR_UNSUPPORTED;
+  const int32_t rows_per_cta = tc ? (kPrefillRows / group) * group : kPrefillRows;
+  const int64_t rows = int64_t(max_queries) * group;
+  const int64_t tiles = (rows + rows_per_cta - 1) / rows_per_cta;
   if (tiles > INT32_MAX) return PA_ERR_UNSUPPORTED;
 
   AttnParams p;
@@ -512,10 +535,10 @@ pa_status pa_prefill(const pa_cache* cache, const void* q, void* out, const int3
   p.mbps = max_blocks_per_seq;
   p.batch = batch;
   p.q_heads = q_heads;
-  p.group = q_heads / cache->kv_heads;
+  p.group = group;
   p.num_queries = max_queries;
   p.rows = int32_t(std::min<int64_t>(rows, INT32_MAX));
-  p.rows_per_cta = kPrefillRows;
+  p.rows_per_cta = rows_per_cta;
   p.row_groups = int32_t(tiles);
   p.max_context_len = max_context_len;
   p.split_tokens = kBlockSize;  // unused: a prefill CTA reads its rows' whole visible context
@@ -525,9 +548,16 @@ pa_status pa_prefill(const pa_cache* cache, const void* q, void* out, const int3
       !make_pool_map(&tv, cache->v, cache->kv_heads, cache->num_blocks))
     return cuda_fail(cudaErrorInvalidValue);
   const dim3 grid(unsigned(tiles), unsigned(cache->kv_heads), unsigned(batch));
-  const cudaError_t e = kernel == PA_KERNEL_MMA
-                            ? launch_attn_prefill(tk, tv, p, grid, static_cast<cudaStream_t>(stream))
-                            : launch_attn_prefill_tc(tk, tv, p, grid, static_cast<cudaStream_t>(stream));
+  const cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  cudaError_t e;
+  if (tc) {
+    CUtensorMap tq;
+    if (!make_query_map(&tq, q, total_queries, q_heads, group, rows_per_cta / group))
+      return cuda_fail(cudaErrorInvalidValue);
+    e = launch_attn_prefill_tc(tk, tv, tq, p, grid, cs);
+  } else {
+    e = launch_attn_prefill(tk, tv, p, grid, cs);
+  }
   return e == cudaSuccess ? PA_OK : cuda_fail(e);
 }
 

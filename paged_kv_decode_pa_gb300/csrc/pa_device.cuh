@@ -230,14 +230,9 @@ struct CtaWork {
 
 // Query tokens of sequence b: uniform (num_queries each) or from query_start
 // (clamped to [0, num_queries] and to the flat arrays; an inconsistent entry
-// raises PA_FLAG_BAD_LENGTH once).
-__device__ __forceinline__ void seq_queries(const AttnParams& p, int b, bool report, int* q0, int* nq) {
-  if (!p.query_start) {
-    *q0 = b * p.num_queries;
-    *nq = p.num_queries;
-    return;
-  }
-  const int a = __ldg(p.query_start + b), e = __ldg(p.query_start + b + 1);
+// raises PA_FLAG_BAD_LENGTH once). query_range takes the two query_start
+// entries already loaded.
+__device__ __forceinline__ void query_range(const AttnParams& p, int a, int e, bool report, int* q0, int* nq) {
   int s = max(0, min(a, p.total_queries)), n = max(0, min(e, p.total_queries) - s);
   if (n > p.num_queries || a < 0 || e < a || e > p.total_queries) {
     if (report) raise_flag(p.status, PA_FLAG_BAD_LENGTH);
@@ -245,6 +240,15 @@ __device__ __forceinline__ void seq_queries(const AttnParams& p, int b, bool rep
   }
   *q0 = s;
   *nq = n;
+}
+
+__device__ __forceinline__ void seq_queries(const AttnParams& p, int b, bool report, int* q0, int* nq) {
+  if (!p.query_start) {
+    *q0 = b * p.num_queries;
+    *nq = p.num_queries;
+    return;
+  }
+  query_range(p, __ldg(p.query_start + b), __ldg(p.query_start + b + 1), report, q0, nq);
 }
 
 // The work of CTA (blockIdx.x = split, .y = KV head, .z = sequence x row

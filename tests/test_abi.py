@@ -151,3 +151,9 @@ def test_prefill_arguments(lib):
     assert _prefill(lib, c, max_q=0) == _lib.PA_ERR_INVALID_ARG
     assert _prefill(lib, c, q=0x30008) == _lib.PA_ERR_INVALID_ARG
     assert _prefill(lib, _cache(dtype=_lib.PA_DTYPE_F32)) == _lib.PA_ERR_UNSUPPORTED
+
+
+def test_prefill_tc_needs_group_of_at_most_128(lib):
+    """The tcgen05 prefill kernel takes whole tokens per 128-row tile."""
+    c = _cache()
+    assert _prefill(lib, c, _lib.PaOptions(0, _lib.PA_KERNEL_TC), hq=2 * 129) == _lib.PA_ERR_UNSUPPORTED

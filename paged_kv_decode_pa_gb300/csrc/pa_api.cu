@@ -26,7 +26,7 @@ cudaError_t launch_cache_write_q8(const pa_cache* c, const void* k_new, const vo
 cudaError_t launch_attn_prefill(const CUtensorMap& tk, const CUtensorMap& tv, const AttnParams& p, dim3 grid,
                                 cudaStream_t stream);
 cudaError_t launch_attn_prefill_tc(const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tq,
-                                   const AttnParams& p, dim3 grid, cudaStream_t stream);
+                                   const AttnParams& p, cudaStream_t stream);
 constexpr int kPrefillRows = 128;  // query rows per prefill CTA
 }  // namespace pa
 
@@ -517,7 +517,7 @@ pa_status pa_prefill(const pa_cache* cache, const void* q, void* out, const int3
   const int32_t rows_per_cta = tc ? (kPrefillRows / group) * group : kPrefillRows;
   const int64_t rows = int64_t(max_queries) * group;
   const int64_t tiles = (rows + rows_per_cta - 1) / rows_per_cta;
-  if (tiles > INT32_MAX) return PA_ERR_UNSUPPORTED;
+  if (tiles * cache->kv_heads * batch > INT32_MAX / 2) return PA_ERR_UNSUPPORTED;
 
   AttnParams p;
   std::memset(&p, 0, sizeof p);
@@ -554,7 +554,7 @@ pa_status pa_prefill(const pa_cache* cache, const void* q, void* out, const int3
     CUtensorMap tq;
     if (!make_query_map(&tq, q, total_queries, q_heads, group, rows_per_cta / group))
       return cuda_fail(cudaErrorInvalidValue);
-    e = launch_attn_prefill_tc(tk, tv, tq, p, grid, cs);
+    e = launch_attn_prefill_tc(tk, tv, tq, p, cs);  // a persistent grid over the same items
   } else {
     e = launch_attn_prefill(tk, tv, p, grid, cs);
   }

@@ -160,7 +160,7 @@ typedef struct pa_options {
 
 #define PA_DEFAULT_SPLIT_TOKENS 1536
 #define PA_LONG_CONTEXT_TOKENS 4096
-#define PA_DEFAULT_SPLIT_LONG 1024
+#define PA_DEFAULT_SPLIT_LONG 1152
 #define PA_DEFAULT_SPLIT_LONG_INT8 768
 
 /*

@@ -134,6 +134,17 @@ __global__ void __launch_bounds__(kMmaThreads, NT == 1 ? 4 : 3)
 
   if (warp == kMmaConsumers) {
     // ---------------- producer ----------------
+    if (p.fused_write && w.t1 > w.L - w.nq) {
+      // This split holds the new tokens: bring their K/V rows (two 128-byte
+      // lines each) into L2 now, so that the consumers' patch does not wait
+      // on memory once per row.
+      for (int e = lane; e < w.nq * 4; e += 32) {
+        const int i = e >> 2, half = e & 1;
+        const void* base_new = (e & 2) ? p.v_new : p.k_new;
+        prefetch_l2(static_cast<const uint16_t*>(base_new) +
+                    (int64_t(w.q0 + i) * p.kv_heads + w.h) * kHeadDim + half * 64);
+      }
+    }
     if (lane == 0) {
       const uint64_t policy = policy_evict_first();
       int issued = 0;

@@ -46,10 +46,11 @@ def test_prefill_64_prompts_of_256(kernel):
 
 
 @pytest.mark.parametrize("kernel", KERNELS)
-@pytest.mark.parametrize("hq,hkv", [(16, 8), (12, 2), (32, 4), (8, 8)])
+@pytest.mark.parametrize("hq,hkv", [(16, 8), (12, 2), (32, 4), (8, 8), (10, 2), (20, 1)])
 def test_prefill_chunks_with_prefixes(hq, hkv, kernel):
-    """Chunks after prefixes of several lengths: tiles of 128 rows, ragged tails,
-    chunk sizes 1 .. 300, context ends inside and at block edges."""
+    """Chunks after prefixes of several lengths: tiles of whole tokens (groups
+    of 1, 2, 5, 6, 8, 20: 125- and 120-row tiles included), ragged tails, chunk
+    sizes 1 .. 300, context ends inside and at block edges."""
     prefixes = (0, 5, 100, 700, 16, 0, 31)
     chunks = (64, 1, 300, 129, 16, 17, 33)
     lens = tuple(p + c for p, c in zip(prefixes, chunks))

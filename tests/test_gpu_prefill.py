@@ -144,3 +144,16 @@ def test_prefill_graph_replay():
     torch.cuda.synchronize()
     ref = oracle.attend_ragged(w.k_cache, w.v_cache, q2, rw.query_start, w.block_tables, lens2, w.scale)
     assert_close(to_f64(pa.to_numpy(out)), ref, "bf16", "prefill graph replay")
+
+
+@pytest.mark.parametrize("hq,kernel", [(64, "tc"), (64, "mma"), (130, "auto")])
+def test_prefill_large_groups(hq, kernel):
+    """One KV head shared by 64 query heads (two tokens per tcgen05 tile), and
+    by 130 (above the tcgen05 kernel's 128: AUTO takes the warp-level kernel)."""
+    prefixes = (0, 37)
+    chunks = (7, 19)
+    lens = tuple(p + c for p, c in zip(prefixes, chunks))
+    w = inputs.custom(batch=2, q_heads=hq, kv_heads=1, context_lens=lens, num_blocks=16, seed=hq,
+                      num_queries=max(chunks))
+    got, ref = _prefill(w, list(chunks), kernel)
+    assert_close(got, ref, "bf16", f"prefill group {hq} ({kernel})")

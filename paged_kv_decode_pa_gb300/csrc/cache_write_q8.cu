@@ -27,17 +27,34 @@ __global__ void __launch_bounds__(kHeadDim)
   const int i = blockIdx.x, h = blockIdx.y, d = threadIdx.x;
   const int warp = d >> 5, lane = d & 31;
   const int64_t num_slots = int64_t(num_blocks) * kBlockSize;
+  // One round trip for what does not depend on the block: this token's slot,
+  // the nearest earlier and later tokens' slots (one per thread), and this
+  // token's own new K and V channel (the row it nearly always writes).
   const int64_t slot = __ldg(slots + i);
+  const int jb = i - 1 - d, jf = i + d;
+  const int64_t sb = jb >= 0 ? __ldg(slots + jb) : -1;
+  const int64_t sf = jf < n ? __ldg(slots + jf) : -1;
+  const float k_own = bf16_lo(uint32_t(__ldg(kn + (int64_t(i) * kv_heads + h) * kHeadDim + d)));
+  const float v_own = bf16_lo(uint32_t(__ldg(vn + (int64_t(i) * kv_heads + h) * kHeadDim + d)));
   if (slot < 0) return;
   if (slot >= num_slots) {
     if (d == 0 && h == 0) raise_flag(status, PA_FLAG_BAD_SLOT);
     return;
   }
   const int64_t block = slot / kBlockSize;
+  // The block's K codes and scale of this thread's channel, requested before
+  // the scans below so that their latency overlaps them.
+  const int64_t blk = int64_t(h) * num_blocks + block;
+  uint8_t* kb = kc + blk * kBlockSize * kHeadDim;
+  const float s_old = ks[blk * kHeadDim + d];
+  uint8_t code[kBlockSize];
+#pragma unroll
+  for (int r = 0; r < kBlockSize; ++r) code[r] = kb[r * kHeadDim + d];
 
   // Leave the block to an earlier token of this call that lands in it.
   // Scanning backwards finds the usual case (the previous token) at once.
-  for (int j0 = i - 1; j0 >= 0; j0 -= kHeadDim) {
+  if (__syncthreads_or(sb >= 0 && sb < num_slots && sb / kBlockSize == block)) return;
+  for (int j0 = i - 1 - kHeadDim; j0 >= 0; j0 -= kHeadDim) {
     const int j = j0 - d;
     bool hit = false;
     if (j >= 0) {
@@ -50,22 +67,22 @@ __global__ void __launch_bounds__(kHeadDim)
   // The last token of the call (in token order) for each row of the block.
   if (d < kBlockSize) s_last[d] = -1;
   __syncthreads();
-  for (int j = i + d; j < n; j += kHeadDim) {
+  if (sf >= 0 && sf < num_slots && sf / kBlockSize == block) atomicMax(&s_last[sf % kBlockSize], jf);
+  for (int j = jf + kHeadDim; j < n; j += kHeadDim) {
     const int64_t sj = __ldg(slots + j);
     if (sj >= 0 && sj < num_slots && sj / kBlockSize == block) atomicMax(&s_last[sj % kBlockSize], j);
   }
   __syncthreads();
 
   // K: this thread's channel over the block's rows.
-  const int64_t blk = int64_t(h) * num_blocks + block;
-  uint8_t* kb = kc + blk * kBlockSize * kHeadDim;
-  const float s_old = ks[blk * kHeadDim + d];
   float x[kBlockSize];
 #pragma unroll
-  for (int r = 0; r < kBlockSize; ++r) x[r] = q8_value(kb[r * kHeadDim + d], s_old);
-#pragma unroll
-  for (int r = 0; r < kBlockSize; ++r)
-    if (s_last[r] >= 0) x[r] = bf16_lo(uint32_t(__ldg(kn + (int64_t(s_last[r]) * kv_heads + h) * kHeadDim + d)));
+  for (int r = 0; r < kBlockSize; ++r) {
+    const int t = s_last[r];
+    x[r] = t < 0    ? q8_value(code[r], s_old)
+           : t == i ? k_own
+                    : bf16_lo(uint32_t(__ldg(kn + (int64_t(t) * kv_heads + h) * kHeadDim + d)));
+  }
   float m = 0.f;
 #pragma unroll
   for (int r = 0; r < kBlockSize; ++r) m = fmaxf(m, fabsf(x[r]));
@@ -76,8 +93,9 @@ __global__ void __launch_bounds__(kHeadDim)
 
   // V: each incoming row on its own scale (the loop condition is uniform).
   for (int r = 0; r < kBlockSize; ++r) {
-    if (s_last[r] < 0) continue;
-    const float v = bf16_lo(uint32_t(__ldg(vn + (int64_t(s_last[r]) * kv_heads + h) * kHeadDim + d)));
+    const int t = s_last[r];
+    if (t < 0) continue;
+    const float v = t == i ? v_own : bf16_lo(uint32_t(__ldg(vn + (int64_t(t) * kv_heads + h) * kHeadDim + d)));
     float a = fabsf(v);
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, off));

@@ -57,22 +57,34 @@ struct Q8Maps {
 // Requantise, in a stage and in the pool, the block at position tok0 for the
 // new tokens it holds (this sequence's tokens at positions >= new0), exactly
 // as the quantised append does; run by the whole producer warp. Lane l owns
-// channels 4l..4l+3. A token whose slot is negative is not written (as in the
-// append); a slot that is not the table slot of its position is a caller
-// error: it raises PA_FLAG_BAD_SLOT and the token is not written. Global
-// loads are issued together (a lane per row's slot, then every new row at
-// once) so that their latencies overlap. Out of line: its registers stay out
-// of the consumers' budget.
+// channels 4l..4l+3; lane t < 16 brings the slot of position tok0 + t (any
+// value where that position holds no new token). A token whose slot is
+// negative is not written (as in the append); a slot that is not the table
+// slot of its position is a caller error: it raises PA_FLAG_BAD_SLOT and the
+// token is not written.
+//
+// This runs once per launch in a few CTAs, late, while the other CTAs stream
+// at the full memory rate, so nearly all of its time goes to first touches:
+// its own instructions and the new rows. It is therefore written as short
+// rolled loops (a 16-way unrolled form measured 15 us on a 32k-context step,
+// of which 12 us disappeared when the same call was repeated), and the
+// producer loads the slots and prefetches the new rows into L1 when the CTA
+// starts. Out of line: its registers stay out of the consumers' budget.
 __device__ __noinline__ void q8_fuse_new_rows(const AttnParams& p, const CtaWork& w, uint8_t* stp, int id,
-                                              int tok0, int lane) {
+                                              int tok0, int slot_in, int lane) {
   const int new0 = w.L - w.nq;
   const int lo = max(tok0, new0), hi = min(tok0 + kBlockSize, w.L);
   const bool in_pool = id >= 0 && id < p.num_blocks;
+  // Row t of this block is new token (tok0 + t - new0); only rows in [lo, hi)
+  // are ever read.
+  const int64_t row_step = int64_t(p.kv_heads) * kHeadDim;
+  const int64_t first = (int64_t(w.q0) + (tok0 - new0)) * row_step + int64_t(w.h) * kHeadDim;
+  const uint16_t* knew = static_cast<const uint16_t*>(p.k_new) + first;
+  const uint16_t* vnew = static_cast<const uint16_t*>(p.v_new) + first;
 
-  // Rows to write: lane t < 16 checks position tok0 + t.
   const int pos = tok0 + lane;
   const bool is_new = lane < kBlockSize && pos >= lo && pos < hi;
-  const int slot = is_new ? __ldg(p.slot_mapping + w.q0 + (pos - new0)) : -1;
+  const int slot = is_new ? slot_in : -1;
   const bool ok = is_new && slot >= 0 && in_pool && slot == id * kBlockSize + lane;
   const uint32_t rows = __ballot_sync(0xffffffffu, ok);
   if (__any_sync(0xffffffffu, is_new && slot >= 0 && !ok) && lane == 0) raise_flag(p.status, PA_FLAG_BAD_SLOT);
@@ -86,55 +98,49 @@ __device__ __noinline__ void q8_fuse_new_rows(const AttnParams& p, const CtaWork
   uint8_t* vpool = static_cast<uint8_t*>(p.v_cache_w) + blk * kQ8TileBytes;
   float* kspool = static_cast<float*>(p.k_scale_w) + blk * kHeadDim;
   float* vspool = static_cast<float*>(p.v_scale_w) + blk * kBlockSize;
-  // Row t of this block is new token (tok0 + t - new0): its 4 channels of lane l.
-  const int64_t row_step = int64_t(p.kv_heads) * kHeadDim;
-  const int64_t first = (int64_t(w.q0) + (tok0 - new0)) * row_step + int64_t(w.h) * kHeadDim + 4 * lane;
-  const uint2* knew = reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(p.k_new) + first);
-  const uint2* vnew = reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(p.v_new) + first);
-  const int64_t step2 = row_step / 4;  // in uint2 units
+  const uint16_t* kmine = knew + 4 * lane;
+  const uint16_t* vmine = vnew + 4 * lane;
 
-  // Every new row's K and V channels of this lane, loaded in one batch (the
-  // rows were prefetched into L2 when the CTA started).
-  uint2 nk[kBlockSize], nv[kBlockSize];
-#pragma unroll
-  for (int t = 0; t < kBlockSize; ++t) {
-    const bool in = rows >> t & 1u;
-    nk[t] = in ? __ldg(knew + t * step2) : make_uint2(0, 0);
-    nv[t] = in ? __ldg(vnew + t * step2) : make_uint2(0, 0);
-  }
-
-  // K: per-channel maxima over the block (old rows dequantised from the stage),
-  // then every row's codes at the new scales.
+  // K: this lane's 4 channels of row t, a new row or an old one dequantised
+  // from the stage.
   const float4 s_old = *reinterpret_cast<const float4*>(ks + 4 * lane);
   const float so[4] = {s_old.x, s_old.y, s_old.z, s_old.w};
-  float x[kBlockSize][4];
-#pragma unroll
-  for (int t = 0; t < kBlockSize; ++t) {
+  auto k_row = [&](int t, float x[4]) {
     if (rows >> t & 1u) {
-      x[t][0] = bf16_lo(nk[t].x);
-      x[t][1] = bf16_hi(nk[t].x);
-      x[t][2] = bf16_lo(nk[t].y);
-      x[t][3] = bf16_hi(nk[t].y);
+      const uint2 u = __ldg(reinterpret_cast<const uint2*>(kmine + t * row_step));
+      x[0] = bf16_lo(u.x);
+      x[1] = bf16_hi(u.x);
+      x[2] = bf16_lo(u.y);
+      x[3] = bf16_hi(u.y);
     } else {
       const uint32_t b4 = *reinterpret_cast<const uint32_t*>(stp + kQ8KOff + q8_off(t, chunk) + within);
 #pragma unroll
-      for (int k = 0; k < 4; ++k) x[t][k] = q8_value(b4 >> (8 * k) & 0xffu, so[k]);
+      for (int k = 0; k < 4; ++k) x[k] = q8_value(b4 >> (8 * k) & 0xffu, so[k]);
     }
+  };
+  // Per-channel maxima over the block, then every row's codes at the new
+  // scales (a lane rewrites only the 4 bytes of each row that it read).
+  float m[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 4
+  for (int t = 0; t < kBlockSize; ++t) {
+    float x[4];
+    k_row(t, x);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) m[k] = fmaxf(m[k], fabsf(x[k]));
   }
   float sn[4], inv[4];
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
-    float m = 0.f;
-#pragma unroll
-    for (int t = 0; t < kBlockSize; ++t) m = fmaxf(m, fabsf(x[t][k]));
-    sn[k] = q8_scale(m);
-    inv[k] = q8_inverse(m);
+    sn[k] = q8_scale(m[k]);
+    inv[k] = q8_inverse(m[k]);
   }
-#pragma unroll
+#pragma unroll 4
   for (int t = 0; t < kBlockSize; ++t) {
+    float x[4];
+    k_row(t, x);
     uint32_t bytes = 0;
 #pragma unroll
-    for (int k = 0; k < 4; ++k) bytes |= q8_code(x[t][k], inv[k]) << (8 * k);
+    for (int k = 0; k < 4; ++k) bytes |= q8_code(x[k], inv[k]) << (8 * k);
     *reinterpret_cast<uint32_t*>(stp + kQ8KOff + q8_off(t, chunk) + within) = bytes;
     *reinterpret_cast<uint32_t*>(kpool + t * kHeadDim + 4 * lane) = bytes;
   }
@@ -142,10 +148,10 @@ __device__ __noinline__ void q8_fuse_new_rows(const AttnParams& p, const CtaWork
   *reinterpret_cast<float4*>(kspool + 4 * lane) = make_float4(sn[0], sn[1], sn[2], sn[3]);
 
   // V: each new row on its own scale.
-#pragma unroll
-  for (int t = 0; t < kBlockSize; ++t) {
-    if (!(rows >> t & 1u)) continue;
-    const float v[4] = {bf16_lo(nv[t].x), bf16_hi(nv[t].x), bf16_lo(nv[t].y), bf16_hi(nv[t].y)};
+  for (uint32_t r = rows; r != 0u; r &= r - 1u) {
+    const int t = __ffs(r) - 1;
+    const uint2 u = __ldg(reinterpret_cast<const uint2*>(vmine + t * row_step));
+    const float v[4] = {bf16_lo(u.x), bf16_hi(u.x), bf16_lo(u.y), bf16_hi(u.y)};
     float mv = fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3])));
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) mv = fmaxf(mv, __shfl_xor_sync(0xffffffffu, mv, off));
@@ -239,16 +245,23 @@ __global__ void __launch_bounds__(kQ8Threads, NT == 1 ? 5 : 3)
 
   if (warp == kQ8Consumers) {
     // ---------------- producer ----------------
+    // The new tokens' slots and rows are needed only at the end of the split:
+    // lane l loads the slot of position f0 + l (the fused blocks span at most
+    // 32 positions) and brings that token's K and V rows into L1 now.
+    const int f0 = w.t0 + nmain * kBlockSize;
+    int fused_slot = -1;
     if (nmain < nblk) {
-      // The new tokens' rows and slots are needed only at the end of the
-      // split: start bringing them into L2 now.
-      const int new0 = w.L - w.nq;
-      for (int pos = max(new0, w.t0); pos < w.t1; ++pos) {
-        const int64_t row = (int64_t(w.q0 + pos - new0) * p.kv_heads + w.h) * kHeadDim + 4 * lane;
-        prefetch_l2(static_cast<const uint16_t*>(p.k_new) + row);
-        prefetch_l2(static_cast<const uint16_t*>(p.v_new) + row);
+      const int new0 = w.L - w.nq, pos = f0 + lane;
+      if (pos >= new0 && pos < w.t1) {
+        fused_slot = __ldg(p.slot_mapping + w.q0 + (pos - new0));
+        const int64_t row = (int64_t(w.q0 + pos - new0) * p.kv_heads + w.h) * kHeadDim;
+        const uint16_t* kr = static_cast<const uint16_t*>(p.k_new) + row;
+        const uint16_t* vr = static_cast<const uint16_t*>(p.v_new) + row;
+        prefetch_l1(kr);
+        prefetch_l1(kr + 64);
+        prefetch_l1(vr);
+        prefetch_l1(vr + 64);
       }
-      if (lane == 0) prefetch_l2(p.slot_mapping + w.q0);
     }
     if (lane == 0) {
       const uint64_t policy = policy_evict_first();
@@ -295,8 +308,9 @@ __global__ void __launch_bounds__(kQ8Threads, NT == 1 ? 5 : 3)
           }
           break;
         }
+        const int slot = __shfl_sync(0xffffffffu, fused_slot, (j - nmain) * kBlockSize + (lane & (kBlockSize - 1)));
         q8_fuse_new_rows(p, w, sbase + Q8Smem::stages + s * kQ8StageBytes, s_ids[j], w.t0 + j * kBlockSize,
-                         lane);
+                         slot, lane);
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(bar_fixed + 8 * (j - nmain));

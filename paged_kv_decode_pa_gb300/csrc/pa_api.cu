@@ -350,12 +350,11 @@ pa_status attend(const pa_cache* cache, const void* q, void* out, const void* k_
 
   cudaError_t e;
   if (int8) {
-    // Quantised append first (it requantises whole blocks), then attention
-    // as its programmatic dependent; the merge follows if there are splits.
     // With one row group per (sequence, KV head) the CTA that holds a new
     // token's block is its only reader, so it requantises the block itself.
-    // With several, the quantised append runs first and attention follows as
-    // its programmatic dependent.
+    // With several, the quantised append (which requantises whole blocks)
+    // runs first and attention follows as its programmatic dependent. The
+    // merge follows if there are splits.
     Q8Maps maps;
     if (!make_q8_maps(&maps, cache)) return cuda_fail(cudaErrorInvalidValue);
     const bool append_first = fused && p.row_groups > 1;

@@ -54,6 +54,10 @@ struct Q8Maps {
   CUtensorMap k, v, ks, vs;
 };
 
+__device__ __forceinline__ void prefetch_l1(const void* ptr) {
+  asm volatile("prefetch.global.L1 [%0];" ::"l"(ptr));
+}
+
 // Requantise, in a stage and in the pool, the block at position tok0 for the
 // new tokens it holds (this sequence's tokens at positions >= new0), exactly
 // as the quantised append does; run by the whole producer warp. Lane l owns

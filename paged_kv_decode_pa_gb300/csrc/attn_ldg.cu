@@ -148,7 +148,13 @@ __global__ void __launch_bounds__(32 * W, ((NT == 1 && PF == 1) ? 12 : 8) / W)
       const int pos = tok0 + row;
       uint4 k4 = make_uint4(0, 0, 0, 0), v4 = make_uint4(0, 0, 0, 0);
       if (row < valid) {
-        if (fused && pos >= new0) {
+        // A new (verify) token is read from the inputs when its slot is the
+        // table slot of its position; otherwise the pool's row stays (a
+        // negative slot is not written).
+        const bool from_new =
+            fused && pos >= new0 && id >= 0 &&
+            __ldg(p.slot_mapping + b * p.num_queries + (pos - new0)) == id * kBlockSize + row;
+        if (from_new) {
           const int64_t src = (int64_t(b * p.num_queries + (pos - new0)) * p.kv_heads + h) * kHeadDim + col * 8;
           k4 = __ldg(reinterpret_cast<const uint4*>(kn + src));
           v4 = __ldg(reinterpret_cast<const uint4*>(vn + src));
@@ -185,8 +191,9 @@ __global__ void __launch_bounds__(32 * W, ((NT == 1 && PF == 1) ? 12 : 8) / W)
             const int64_t dst =
                 ((int64_t(h) * p.num_blocks + s_id / kBlockSize) * kBlockSize + s_id % kBlockSize) * kHeadDim +
                 col * 8;
-            *reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.k_cache_w) + dst) = v[e];
-            *reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.v_cache_w) + dst) = v[8 + e];
+            const int64_t src = (int64_t(b * p.num_queries + (pos - new0)) * p.kv_heads + h) * kHeadDim + col * 8;
+            *reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.k_cache_w) + dst) = __ldg(reinterpret_cast<const uint4*>(kn + src));
+            *reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.v_cache_w) + dst) = __ldg(reinterpret_cast<const uint4*>(vn + src));
           } else if (s_id >= 0 && col == 0) {
             raise_flag(p.status, PA_FLAG_BAD_SLOT);
           }

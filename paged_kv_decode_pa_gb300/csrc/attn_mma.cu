@@ -33,6 +33,12 @@
 // Fused verify: the CTA whose split holds a new token's position writes that
 // token's K/V row to the cache (row group 0 only) and patches the row into its
 // shared-memory tile from the inputs, so no CTA depends on another's write.
+// The producer warp does the patching: a block holding new tokens lands on a
+// barrier of its own, the producer patches the stage and then completes the
+// stage's full barrier, so the consumers carry no code for it. A new token
+// whose slot is not the table slot of its position (a negative slot is not
+// written) keeps the pool's row, as a separate append followed by attention
+// would see it.
 #include "mma_tile.cuh"
 
 namespace pa {
@@ -49,8 +55,8 @@ constexpr int kMmaThreads = (kMmaConsumers + 1) * 32;
 struct MmaSmem {
   // Offsets from the 1024-byte aligned base.
   static constexpr int stages = 0;
-  static constexpr int bars = kStages * kStageBytes;            // full[kStages], empty[kStages]
-  static constexpr int ids = bars + 2 * kStages * 8;            // block ids of the split
+  static constexpr int bars = kStages * kStageBytes;            // full, empty, landed [kStages] each
+  static constexpr int ids = bars + 3 * kStages * 8;            // block ids of the split
   static constexpr int ml = ids + (kMaxSplitTokens / kBlockSize) * 4;  // m, l per warp and row
   static constexpr int flag = ml + 2 * kMmaConsumers * kRowSlots * 4;
   static constexpr int total = flag + 16;
@@ -78,6 +84,7 @@ __global__ void __launch_bounds__(kMmaThreads, NT == 1 ? 4 : 3)
   int* s_flag = reinterpret_cast<int*>(sbase + MmaSmem::flag);
   const uint32_t bar_full = base + MmaSmem::bars;
   const uint32_t bar_empty = bar_full + kStages * 8;
+  const uint32_t bar_land = bar_empty + kStages * 8;  // blocks holding new tokens land here
 
   // The descriptor fetch overlaps the loads below instead of delaying the
   // first TMA issue.
@@ -120,6 +127,7 @@ __global__ void __launch_bounds__(kMmaThreads, NT == 1 ? 4 : 3)
     for (int s = 0; s < kStages; ++s) {
       mbar_init(bar_full + 8 * s, 1);
       mbar_init(bar_empty + 8 * s, 1);
+      mbar_init(bar_land + 8 * s, 1);
     }
     fence_mbar_init();
   }
@@ -134,41 +142,113 @@ __global__ void __launch_bounds__(kMmaThreads, NT == 1 ? 4 : 3)
 
   if (warp == kMmaConsumers) {
     // ---------------- producer ----------------
-    if (p.fused_write && w.t1 > w.L - w.nq) {
+    // Blocks from jf on hold new tokens: they land on bar_land, and the whole
+    // warp's patch_next() turns them into ordinary stages.
+    const int new0 = w.L - w.nq;
+    const int jf = (p.fused_write && w.t1 > new0) ? max(0, new0 - w.t0) / kBlockSize : nblk;
+    if (jf < nblk) {
       // This split holds the new tokens: bring their K/V rows (two 128-byte
-      // lines each) into L2 now, so that the consumers' patch does not wait
-      // on memory once per row.
+      // lines each) and their slots into L2 now, so that the patch does not
+      // wait on memory once per row.
       for (int e = lane; e < w.nq * 4; e += 32) {
         const int i = e >> 2, half = e & 1;
         const void* base_new = (e & 2) ? p.v_new : p.k_new;
         prefetch_l2(static_cast<const uint16_t*>(base_new) +
                     (int64_t(w.q0 + i) * p.kv_heads + w.h) * kHeadDim + half * 64);
       }
+      if (lane == 0) prefetch_l2(p.slot_mapping + w.q0);
+    }
+    int patched = jf;  // next block holding new tokens to patch
+    // Patch block `patched` once it has landed: the new tokens' rows whose
+    // slot is the table slot of their position come from the inputs; row
+    // group 0 writes every in-pool slot to the cache; V rows past the
+    // context are zeroed. Then the stage's full barrier completes.
+    auto patch_next = [&]() -> bool {
+      const int k = patched, s = k % kStages;
+      if (!__all_sync(0xffffffffu, mbar_wait(bar_land + 8 * s, ((k - jf) / kStages) & 1))) return false;
+      uint8_t* kt_ptr = sbase + MmaSmem::stages + s * kStageBytes;
+      uint8_t* vt_ptr = kt_ptr + kTileBytes;
+      const int tok0 = w.t0 + k * kBlockSize;
+      const int pos_lo = max(tok0, new0), pos_hi = min(tok0 + kBlockSize, w.L);
+      const int id = s_ids[k];
+      const bool id_ok = id >= 0 && id < p.num_blocks;
+      const int ch = lane & 15;  // lanes 0..15 move K chunks, lanes 16..31 V chunks
+      const bool is_v = lane >= 16;
+      for (int pos = pos_lo; pos < pos_hi; ++pos) {
+        const int i = pos - new0, t = pos - tok0;
+        const int slot = __ldg(p.slot_mapping + w.q0 + i);
+        const int64_t src = (int64_t(w.q0 + i) * p.kv_heads + w.h) * kHeadDim + ch * 8;
+        const uint4 val =
+            __ldg(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(is_v ? p.v_new : p.k_new) + src));
+        if (id_ok && slot == id * kBlockSize + t)
+          *reinterpret_cast<uint4*>((is_v ? vt_ptr : kt_ptr) + tile_off(t, ch)) = val;
+        if (w.rg == 0) {
+          if (slot >= 0 && slot < p.num_blocks * kBlockSize) {
+            const int64_t dst =
+                ((int64_t(w.h) * p.num_blocks + slot / kBlockSize) * kBlockSize + slot % kBlockSize) * kHeadDim +
+                ch * 8;
+            *reinterpret_cast<uint4*>(static_cast<uint16_t*>(is_v ? p.v_cache_w : p.k_cache_w) + dst) = val;
+          } else if (slot >= 0 && lane == 0) {
+            raise_flag(p.status, PA_FLAG_BAD_SLOT);
+          }
+        }
+      }
+      const int valid = min(kBlockSize, w.L - tok0);
+      for (int e = lane; e < (kBlockSize - valid) * 16; e += 32) {
+        const int t = valid + (e >> 4), c16 = e & 15;
+        *reinterpret_cast<uint4*>(vt_ptr + tile_off(t, c16)) = make_uint4(0, 0, 0, 0);
+      }
+      // These generic writes come before the next tensor load into the stage.
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_full + 8 * s);
+      ++patched;
+      return true;
+    };
+    // Lane 0 issues the loads. A block that holds new tokens lands on
+    // bar_land; its stage can be reused only once it is patched, so lane 0
+    // runs ahead to kStages blocks past the first of them, and the whole warp
+    // then patches them in order, issuing one more block after each patch
+    // when there are more (over 80 new tokens in the split).
+    const uint64_t policy = policy_evict_first();
+    auto issue = [&](int j) -> bool {  // lane 0
+      const int s = j % kStages, n = j / kStages;
+      if (n > 0 && !mbar_wait(bar_empty + 8 * s, (n - 1) & 1)) return false;
+      const uint32_t st = base + MmaSmem::stages + s * kStageBytes;
+      const uint32_t fb = (j >= jf ? bar_land : bar_full) + 8 * s;
+      int id = s_ids[j];
+      if (id < 0 || id >= p.num_blocks) {  // outside the pool: TMA reads zeros instead
+        raise_flag(p.status, PA_FLAG_BAD_BLOCK);
+        id = -1;
+      }
+      const int y = id >= 0 ? id * kBlockSize : -kBlockSize;
+      mbar_arrive_expect_tx(fb, kStageBytes);
+      tma_load_3d(st, &tmap_k, 0, y, w.h, fb, policy);
+      tma_load_3d(st + kHalfTile, &tmap_k, 64, y, w.h, fb, policy);
+      tma_load_3d(st + kTileBytes, &tmap_v, 0, y, w.h, fb, policy);
+      tma_load_3d(st + kTileBytes + kHalfTile, &tmap_v, 64, y, w.h, fb, policy);
+      return true;
+    };
+    int issued = 0;
+    bool ok = true;
+    if (lane == 0) {
+      const int ahead = min(nblk, jf + kStages);
+      while (issued < ahead && (ok = issue(issued))) ++issued;
+    }
+    issued = __shfl_sync(0xffffffffu, issued, 0);
+    ok = __shfl_sync(0xffffffffu, ok, 0);
+    while (ok && patched < issued) {
+      ok = patch_next();
+      if (ok && issued < nblk) {
+        if (lane == 0 && (ok = issue(issued))) ++issued;
+        issued = __shfl_sync(0xffffffffu, issued, 0);
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+      }
     }
     if (lane == 0) {
-      const uint64_t policy = policy_evict_first();
-      int issued = 0;
-      for (int j = 0; j < nblk; ++j) {
-        const int s = j % kStages, n = j / kStages;
-        if (n > 0 && !mbar_wait(bar_empty + 8 * s, (n - 1) & 1)) {
-          raise_flag(p.status, PA_FLAG_TIMEOUT);
-          s_flag[2] = 1;
-          break;
-        }
-        const uint32_t st = base + MmaSmem::stages + s * kStageBytes;
-        const uint32_t fb = bar_full + 8 * s;
-        int id = s_ids[j];
-        if (id < 0 || id >= p.num_blocks) {  // outside the pool: TMA reads zeros instead
-          raise_flag(p.status, PA_FLAG_BAD_BLOCK);
-          id = -1;
-        }
-        const int y = id >= 0 ? id * kBlockSize : -kBlockSize;
-        mbar_arrive_expect_tx(fb, kStageBytes);
-        tma_load_3d(st, &tmap_k, 0, y, w.h, fb, policy);
-        tma_load_3d(st + kHalfTile, &tmap_k, 64, y, w.h, fb, policy);
-        tma_load_3d(st + kTileBytes, &tmap_v, 0, y, w.h, fb, policy);
-        tma_load_3d(st + kTileBytes + kHalfTile, &tmap_v, 64, y, w.h, fb, policy);
-        issued = j + 1;
+      if (!ok) {
+        raise_flag(p.status, PA_FLAG_TIMEOUT);
+        s_flag[2] = 1;
       }
       s_flag[1] = issued;
     }
@@ -216,39 +296,12 @@ __global__ void __launch_bounds__(kMmaThreads, NT == 1 ? 4 : 3)
       uint8_t* vt_ptr = kt_ptr + kTileBytes;
       const int tok0 = w.t0 + j * kBlockSize;
 
-      // Fix the tile up in shared memory before reading it.
+      // Zero the V rows past the context, so that 0 x (stale row) stays 0.
+      // The producer has done so, and patched the tile, for a block holding
+      // new tokens.
       bool patched = false;
       const int valid = min(kBlockSize, w.L - tok0);  // rows of this block inside the context
-      if (p.fused_write && tok0 + kBlockSize > new0) {
-        // New tokens: K/V come from the inputs; row group 0 also writes them
-        // to the cache. Lanes 0..15 move K chunks, lanes 16..31 V chunks.
-        const int pos_lo = max(tok0, new0), pos_hi = min(tok0 + kBlockSize, w.L);
-        const int ch = lane & 15;
-        const bool is_v = lane >= 16;
-        for (int pos = pos_lo; pos < pos_hi; ++pos) {
-          const int i = pos - new0;
-          const int t = pos - tok0;
-          const int64_t src =
-              (int64_t(w.q0 + i) * p.kv_heads + w.h) * kHeadDim + ch * 8;
-          const uint16_t* srcp = static_cast<const uint16_t*>(is_v ? p.v_new : p.k_new) + src;
-          const uint4 val = __ldg(reinterpret_cast<const uint4*>(srcp));
-          *reinterpret_cast<uint4*>((is_v ? vt_ptr : kt_ptr) + tile_off(t, ch)) = val;
-          if (w.rg == 0) {
-            const int slot = __ldg(p.slot_mapping + w.q0 + i);
-            if (slot >= 0 && slot < p.num_blocks * kBlockSize) {
-              const int64_t dst = ((int64_t(w.h) * p.num_blocks + slot / kBlockSize) * kBlockSize +
-                                   slot % kBlockSize) * kHeadDim + ch * 8;
-              uint16_t* cache = static_cast<uint16_t*>(is_v ? p.v_cache_w : p.k_cache_w);
-              *reinterpret_cast<uint4*>(cache + dst) = val;
-            } else if (slot >= 0 && lane == 0) {
-              raise_flag(p.status, PA_FLAG_BAD_SLOT);
-            }
-          }
-        }
-        patched = true;
-      }
-      if (valid < kBlockSize) {
-        // Rows beyond the context: zero V so that 0 x (stale row) stays 0.
+      if (valid < kBlockSize && !(p.fused_write && tok0 + kBlockSize > new0)) {
         for (int e = lane; e < (kBlockSize - valid) * 16; e += 32) {
           const int t = valid + (e >> 4), ch = e & 15;
           *reinterpret_cast<uint4*>(vt_ptr + tile_off(t, ch)) = make_uint4(0, 0, 0, 0);
@@ -276,8 +329,14 @@ __global__ void __launch_bounds__(kMmaThreads, NT == 1 ? 4 : 3)
     // CTA leaves, and write nothing.
     if (threadIdx.x == 0) {
       const int issued = s_flag[1];
-      for (int j = max(0, issued - kStages); j < issued; ++j)
-        (void)mbar_wait(bar_full + 8 * (j % kStages), (j / kStages) & 1);
+      const int new0 = w.L - w.nq;
+      const int jf = (p.fused_write && w.t1 > new0) ? max(0, new0 - w.t0) / kBlockSize : nblk;
+      for (int j = max(0, issued - kStages); j < issued; ++j) {
+        if (j >= jf)
+          (void)mbar_wait(bar_land + 8 * (j % kStages), ((j - jf) / kStages) & 1);
+        else
+          (void)mbar_wait(bar_full + 8 * (j % kStages), (j / kStages) & 1);
+      }
     }
     __syncthreads();
     return;

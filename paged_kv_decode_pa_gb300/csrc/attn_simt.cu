@@ -92,14 +92,22 @@ __global__ void __launch_bounds__(kSimtThreads) attn_simt_kernel(const AttnParam
     for (int t = 0; t < ntok; ++t) {
       const int pos = tok0 + t;
       float k[4] = {0.f, 0.f, 0.f, 0.f}, v[4] = {0.f, 0.f, 0.f, 0.f};
+      const int slot = (p.fused_write && pos >= new0) ? __ldg(p.slot_mapping + w.q0 + (pos - new0)) : -1;
       if (p.fused_write && pos >= new0) {
-        // A new (verify) token: read it from the inputs; row group 0 writes it.
+        // A new (verify) token: read from the inputs when its slot is the
+        // table slot of its position, else from the pool (a negative slot is
+        // not written); row group 0 writes every in-pool slot.
         const int i = pos - new0;
         const int64_t src = (int64_t(w.q0 + i) * p.kv_heads + w.h) * kHeadDim + d0;
-        Vec4<T>::load(static_cast<const T*>(p.k_new) + src, k);
-        Vec4<T>::load(static_cast<const T*>(p.v_new) + src, v);
+        if (id_ok && slot == id * kBlockSize + t) {
+          Vec4<T>::load(static_cast<const T*>(p.k_new) + src, k);
+          Vec4<T>::load(static_cast<const T*>(p.v_new) + src, v);
+        } else if (id_ok) {
+          const int64_t off = ((int64_t(w.h) * p.num_blocks + id) * kBlockSize + t) * kHeadDim + d0;
+          Vec4<T>::load_plain(kc + off, k);
+          Vec4<T>::load_plain(vc + off, v);
+        }
         if (w.rg == 0) {
-          const int slot = __ldg(p.slot_mapping + w.q0 + i);
           if (slot >= 0 && slot < p.num_blocks * kBlockSize) {
             const int64_t dst =
                 ((int64_t(w.h) * p.num_blocks + slot / kBlockSize) * kBlockSize + slot % kBlockSize) *

@@ -146,3 +146,23 @@ def test_q8_verify_shapes(nq, hq, hkv):
         out, dev = _gpu_q8(w, pool, verify=True, split=split)
         _same_pool(dev, ref_pool, f"verify nq={nq} {hq}/{hkv} split {split}")
         assert_close(to_f64(out), ref, "bf16", f"int8 verify nq={nq} {hq}/{hkv} split {split}")
+
+
+@pytest.mark.parametrize("hq,hkv", [(16, 8), (32, 4)])
+def test_q8_verify_negative_slots(hq, hkv):
+    """int8 pool: a new token with a negative slot is not written and its
+    position keeps the pool's row, in the fused requantisation (one row group)
+    and behind the separate append (two row groups)."""
+    nq = 4
+    w = inputs.custom(batch=4, q_heads=hq, kv_heads=hkv, context_lens=(4, 17, 33, 300), num_blocks=64,
+                      seed=8765 + hq, num_queries=nq)
+    slots = w.slot_mapping.copy()
+    slots[[1, 4, 5, 15]] = -1
+    w.slot_mapping = slots
+    pool = inputs.q8_pool(w)
+    ref_pool = _oracle_pool(pool)
+    ref = oracle.verify_q8(*ref_pool, w.q, w.k_new, w.v_new, w.slot_mapping, w.block_tables,
+                           w.context_lens, w.scale)
+    out, dev = _gpu_q8(w, pool, verify=True)
+    _same_pool(dev, ref_pool, f"negative slots {hq}/{hkv}")
+    assert_close(to_f64(out), ref, "bf16", f"int8 negative slots {hq}/{hkv}")

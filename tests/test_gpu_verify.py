@@ -54,3 +54,27 @@ def test_one_query_verify_equals_write_then_decode():
     ver, vk, vv = gpu_verify(v)
     assert vk.tobytes() == dk.tobytes() and vv.tobytes() == dv.tobytes()
     assert np.array_equal(ver[:, 0], dec), "fused one-token verify must equal write + decode bit for bit"
+
+
+def _with_negative_slots(w, which):
+    slots = w.slot_mapping.copy()
+    slots[list(which)] = -1
+    w.slot_mapping = slots
+    return w
+
+
+@pytest.mark.parametrize("kernel", ["auto", "mma_ldg", "simt"])
+@pytest.mark.parametrize("hq,hkv", [(16, 8), (32, 4)])
+def test_verify_negative_slots(kernel, hq, hkv):
+    """A new token with a negative slot is not written, and attention sees the
+    pool's row at its position: the fused call equals the append (which skips
+    the token) followed by attention over the pool. One and two row groups."""
+    nq = 4
+    w = inputs.custom(batch=4, q_heads=hq, kv_heads=hkv, context_lens=(4, 17, 33, 300), num_blocks=64,
+                      dtype="bf16", seed=4321 + hq, num_queries=nq)
+    # Sequence 0's second token, sequence 1's first two, sequence 3's last.
+    w = _with_negative_slots(w, (1, 4, 5, 15))
+    ref, okc, ovc = oracle_verify_of(w)
+    out, gk, gv = gpu_verify(w, kernel=kernel)
+    assert gk.tobytes() == okc.tobytes() and gv.tobytes() == ovc.tobytes()
+    assert_close(to_f64(out), ref, "bf16", f"negative slots {hq}/{hkv} {kernel}")

@@ -166,3 +166,21 @@ def test_q8_verify_negative_slots(hq, hkv):
     out, dev = _gpu_q8(w, pool, verify=True)
     _same_pool(dev, ref_pool, f"negative slots {hq}/{hkv}")
     assert_close(to_f64(out), ref, "bf16", f"int8 negative slots {hq}/{hkv}")
+
+
+def test_q8_verify_many_new_tokens():
+    """int8 pool, 100 new tokens per sequence (several row groups: the append
+    runs first), some with negative slots."""
+    nq = 100
+    w = inputs.custom(batch=3, q_heads=4, kv_heads=4, context_lens=(100, 150, 700), num_blocks=80,
+                      seed=1357, num_queries=nq)
+    slots = w.slot_mapping.copy()
+    slots[[7, 99, 150, 298]] = -1
+    w.slot_mapping = slots
+    pool = inputs.q8_pool(w)
+    ref_pool = _oracle_pool(pool)
+    ref = oracle.verify_q8(*ref_pool, w.q, w.k_new, w.v_new, w.slot_mapping, w.block_tables,
+                           w.context_lens, w.scale)
+    out, dev = _gpu_q8(w, pool, verify=True)
+    _same_pool(dev, ref_pool, "100 new tokens")
+    assert_close(to_f64(out), ref, "bf16", "int8 100 new tokens")

@@ -78,3 +78,19 @@ def test_verify_negative_slots(kernel, hq, hkv):
     out, gk, gv = gpu_verify(w, kernel=kernel)
     assert gk.tobytes() == okc.tobytes() and gv.tobytes() == ovc.tobytes()
     assert_close(to_f64(out), ref, "bf16", f"negative slots {hq}/{hkv} {kernel}")
+
+
+@pytest.mark.parametrize("kernel", ["auto", "mma_ldg", "simt"])
+@pytest.mark.parametrize("split", [0, 48])
+def test_verify_many_new_tokens(kernel, split):
+    """100 new tokens per sequence, one query head per KV head: seven row
+    groups, and (unsplit) more blocks holding new tokens than a CTA's ring has
+    stages. Some new tokens have negative slots."""
+    nq = 100
+    w = inputs.custom(batch=3, q_heads=4, kv_heads=4, context_lens=(100, 150, 700), num_blocks=80,
+                      dtype="bf16", seed=2468, num_queries=nq)
+    w = _with_negative_slots(w, (7, 99, 100 + 50, 200 + 98))
+    ref, okc, ovc = oracle_verify_of(w)
+    out, gk, gv = gpu_verify(w, kernel=kernel, split_tokens=split)
+    assert gk.tobytes() == okc.tobytes() and gv.tobytes() == ovc.tobytes()
+    assert_close(to_f64(out), ref, "bf16", f"100 new tokens {kernel} split {split}")

@@ -94,3 +94,19 @@ def test_ragged_all_decode_equals_decode():
     rw = inputs.ragged(w, [1] * 12)
     got, ref = _run(rw)
     assert_close(got, ref, "bf16", "ragged, all decode")
+
+
+@pytest.mark.parametrize("kv,hq,hkv", [("native", 16, 8), ("native", 32, 4), ("int8", 16, 8), ("int8", 12, 2)])
+def test_ragged_negative_slots(kv, hq, hkv):
+    """Some new tokens of a ragged call have negative slots: not written, and
+    attention sees the pool's rows at their positions (the fused write equals
+    the append followed by attention)."""
+    lens = (5, 16, 17, 18, 47, 48, 49, 300, 513, 1, 64)
+    w = inputs.custom(batch=len(lens), q_heads=hq, kv_heads=hkv, context_lens=lens, num_blocks=120,
+                      seed=hq * 10 + hkv + 7, num_queries=5)
+    rw = inputs.ragged(w, [min(n, L) for n, L in zip(MIX, lens)])
+    slots = rw.slot_mapping.copy()
+    slots[[0, 3, 9, 17]] = -1  # tokens of sequences 0, 1, 5 and 7
+    rw.slot_mapping = slots
+    got, ref = _run(rw, kv=kv)
+    assert_close(got, ref, "bf16", f"ragged negative slots {kv} {hq}/{hkv}")

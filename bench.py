@@ -18,7 +18,9 @@ step. rank 0 prints one JSON line.
                     [--workload c4] [--no-extra]
 
 --impl reference times the fp64 CPU oracle (the only reference this method
-has) on a bounded sample of the same workload, on the host cores.
+has) on a bounded sample of the same workload, on the host cores. --prefill
+times the paged prefill workloads alone; --floor times the fixed cost of one
+call under these events; --record-traffic stores an ncu capture's DRAM bytes.
 """
 
 from __future__ import annotations
@@ -74,6 +76,9 @@ def parse_args():
     ap.add_argument("--prefill", action="store_true",
                     help="time only the paged prefill workloads (both kernels, --steps calls each) and print "
                          "their line")
+    ap.add_argument("--floor", action="store_true",
+                    help="time the fixed cost of one call under the bench's events (empty event pair, one-element "
+                         "kernels, back-to-back c3 calls, c3 at equal lengths) and print its line")
     return ap.parse_args()
 
 
@@ -853,12 +858,57 @@ def run_prefill_only(args):
                       "dtype": "bf16", "data": "synthetic", "per_config": res}), flush=True)
 
 
+def run_floor(args):
+    """One JSON line: medians (us) of what the bench's CUDA events measure
+    around nothing, around one-element torch kernels, around one to three
+    back-to-back c3 decode steps, and around the c3 step with all lengths set
+    to 16 or to 384 tokens. Each timed region follows the same L2 flush and
+    device-side hold as the bench's own steps."""
+    import torch
+
+    device = torch.device("cuda", 0)
+    torch.cuda.set_device(device)
+    flush = make_l2_flush(device)
+    x = torch.zeros(1, device=device)
+    n = max(10, args.steps)
+
+    def median_us(fn):
+        for _ in range(3):
+            flush()
+            fn()
+        torch.cuda.synchronize()
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(n)]
+        for k in range(n):
+            flush()
+            gpu_hold()
+            ev[k][0].record()
+            fn()
+            ev[k][1].record()
+        torch.cuda.synchronize()
+        return round(statistics.median(e[0].elapsed_time(e[1]) * 1e3 for e in ev), 2)
+
+    res = {"empty_event_pair": median_us(lambda: None),
+           "one_element_kernel_x1": median_us(lambda: x.add_(1)),
+           "one_element_kernel_x10": median_us(lambda: [x.add_(1) for _ in range(10)])}
+    for name, kw in (("c3", {}), ("c3_len16", {"context_lens": (16,) * 64, "len_range": (0, 0)}),
+                     ("c3_len384", {"context_lens": (384,) * 64, "len_range": (0, 0)})):
+        st = DecodeStep(inputs.make("c3", **kw), device)
+        res[name + "_x1"] = median_us(st.attend)
+        if name == "c3":
+            res[name + "_x2"] = median_us(lambda: (st.attend(), st.attend()))
+            res[name + "_x3"] = median_us(lambda: (st.attend(), st.attend(), st.attend()))
+    print(json.dumps({"metric": "fixed cost of one call under the bench's CUDA events", "unit": "us",
+                      "steps": n, "data": "synthetic", "per_config": res}), flush=True)
+
+
 def main():
     args = parse_args()
     if args.record_traffic:
         print(json.dumps(record_traffic(*args.record_traffic)))
     elif args.prefill:
         run_prefill_only(args)
+    elif args.floor:
+        run_floor(args)
     elif args.impl == "reference":
         run_reference(args)
     else:

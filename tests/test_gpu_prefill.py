@@ -3,6 +3,8 @@ the oracle, bf16."""
 
 from __future__ import annotations
 
+import functools
+
 import numpy as np
 import pytest
 
@@ -157,3 +159,50 @@ def test_prefill_large_groups(hq, kernel):
                       num_queries=max(chunks))
     got, ref = _prefill(w, list(chunks), kernel)
     assert_close(got, ref, "bf16", f"prefill group {hq} ({kernel})")
+
+
+_LONG = dict(batch=8, q_heads=12, kv_heads=2, context_lens=(4096,) * 8, num_blocks=2100, seed=61, num_queries=2048)
+# Sampled rows of the long workload: (sequence, first row of its chunk, rows).
+# The chunk's first rows see the shortest contexts, its last rows the longest.
+_LONG_SAMPLES = ((0, 0, 256), (7, 1536, 512))
+
+
+@functools.lru_cache(maxsize=1)
+def _long_reference():
+    """The oracle's rows for _LONG_SAMPLES. A chunk's rows are its sequence's
+    last positions, so rows [r0, r0 + n) of a 2048-token chunk ending at 4096
+    are those of an n-token chunk ending at 2048 + r0 + n."""
+    w = inputs.custom(**_LONG)
+    rw = inputs.ragged(w, [2048] * 8)
+    refs = []
+    for b, r0, n in _LONG_SAMPLES:
+        q0 = int(rw.query_start[b]) + r0
+        refs.append(oracle.attend_ragged(w.k_cache, w.v_cache, rw.q[q0:q0 + n], np.array([0, n], dtype=np.int32),
+                                         w.block_tables[b:b + 1], np.array([2048 + r0 + n], dtype=np.int32),
+                                         w.scale))
+    return refs
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_prefill_long_chunks_full_size(kernel):
+    """The benchmark's long workload at full size (8 sequences, 2048-token
+    chunks after 2048-token prefixes, 12/2 heads), in the benchmark's launch
+    configuration; the oracle checks sampled rows of two sequences."""
+    import torch
+
+    import paged_kv_decode_pa_gb300 as pa
+
+    w = inputs.custom(**_LONG)
+    rw = inputs.ragged(w, [2048] * 8)
+    dev = torch.device("cuda")
+    kc, vc = pa.to_torch(w.k_cache, dev), pa.to_torch(w.v_cache, dev)
+    ws = torch.zeros(256, dtype=torch.uint8, device=dev)
+    out = pa.pa_prefill(kc, vc, pa.to_torch(rw.q, dev), pa.to_torch(rw.query_start, dev),
+                        pa.to_torch(w.block_tables, dev), pa.to_torch(w.context_lens, dev), w.max_context_len,
+                        w.scale, rw.max_queries, workspace=ws, kernel=kernel)
+    torch.cuda.synchronize()
+    assert pa.pa_workspace_status(ws) == 0
+    got = to_f64(pa.to_numpy(out))
+    for (b, r0, n), ref in zip(_LONG_SAMPLES, _long_reference()):
+        q0 = int(rw.query_start[b]) + r0
+        assert_close(got[q0:q0 + n], ref, "bf16", f"prefill 8 x 2048 after 2048, sequence {b} rows {r0}+{n} ({kernel})")

@@ -19,8 +19,8 @@ step. rank 0 prints one JSON line.
 
 --impl reference times the fp64 CPU oracle (the only reference this method
 has) on a bounded sample of the same workload, on the host cores. --prefill
-times the paged prefill workloads alone; --floor times the fixed cost of one
-call under these events; --record-traffic stores an ncu capture's DRAM bytes.
+times the paged prefill workloads alone; --record-traffic stores an ncu
+capture's DRAM bytes.
 """
 
 from __future__ import annotations
@@ -58,9 +58,7 @@ def parse_args():
     ap.add_argument("--kv", default="bf16", choices=["bf16", "int8"],
                     help="KV pool format (int8: bytes + scales, dequantised inside the kernel)")
     ap.add_argument("--no-extra", action="store_true", help="skip the per_config measurements")
-    ap.add_argument("--kernel", default="auto", choices=["auto", "mma", "mma_ldg", "simt"])
-    ap.add_argument("--prefetch", type=int, default=0, help="blocks in flight per warp (mma_ldg kernel)")
-    ap.add_argument("--warps", type=int, default=0, help="warps per split (mma_ldg kernel)")
+    ap.add_argument("--kernel", default="auto", choices=["auto", "mma", "simt"])
     ap.add_argument("--split-tokens", type=int, default=0)
     ap.add_argument("--buckets", action="store_true",
                     help="also time the Qwen2-shaped decode step per batch bucket (1..64), direct and as "
@@ -76,9 +74,6 @@ def parse_args():
     ap.add_argument("--prefill", action="store_true",
                     help="time only the paged prefill workloads (both kernels, --steps calls each) and print "
                          "their line")
-    ap.add_argument("--floor", action="store_true",
-                    help="time the fixed cost of one call under the bench's events (empty event pair, one-element "
-                         "kernels, back-to-back c3 calls, c3 at equal lengths) and print its line")
     return ap.parse_args()
 
 
@@ -292,7 +287,7 @@ class DecodeStep:
     the two calls. A verify workload's step is pa_verify.
     """
 
-    def __init__(self, w, device, split_tokens=0, kernel="auto", prefetch=0, warps=0, fused=True, kv="bf16"):
+    def __init__(self, w, device, split_tokens=0, kernel="auto", fused=True, kv="bf16"):
         import paged_kv_decode_pa_gb300 as pa
 
         self.pa = pa
@@ -301,8 +296,6 @@ class DecodeStep:
         self.dev = device
         self.split = split_tokens
         self.kernel = kernel
-        self.prefetch = prefetch
-        self.warps = warps
         self.scales = {}
         if kv == "int8":  # a seeded int8 pool for the same tables and lengths
             pool = inputs.q8_pool(w)
@@ -345,13 +338,11 @@ class DecodeStep:
         w = self.w
         if not self.fused:
             self.pa.pa_decode(self.kc, self.vc, self.q, self.tables, self.lens, w.max_context_len, w.scale,
-                              self.ws, out=self.out, split_tokens=self.split, kernel=self.kernel,
-                              prefetch=self.prefetch, warps=self.warps, **self.scales)
+                              self.ws, out=self.out, split_tokens=self.split, kernel=self.kernel, **self.scales)
         else:
             self.pa.pa_verify(self.kc, self.vc, self.q4, self.k_new, self.v_new, self.slots, self.tables,
                               self.lens, w.max_context_len, w.scale, self.ws, out=self.out4,
-                              split_tokens=self.split, kernel=self.kernel, prefetch=self.prefetch,
-                              warps=self.warps, **self.scales)
+                              split_tokens=self.split, kernel=self.kernel, **self.scales)
 
     def run(self):
         """One whole step."""
@@ -615,7 +606,7 @@ def launches_per_step(w, step, split: int, kernel: str, kv: str) -> int:
         size = _lib.PA_DEFAULT_SPLIT_TOKENS
     splits = max(1, -(-max_ctx // size))
     n = (0 if step.fused else 1) + 1
-    tensor_core = kv == "int8" or (kernel in ("auto", "mma", "mma_ldg") and s.dtype == "bf16")
+    tensor_core = kv == "int8" or (kernel in ("auto", "mma") and s.dtype == "bf16")
     if tensor_core and splits > 1:
         n += 1
     rows = s.num_queries * (s.q_heads // s.kv_heads)
@@ -624,10 +615,9 @@ def launches_per_step(w, step, split: int, kernel: str, kv: str) -> int:
     return n
 
 
-def measure_extra(name, device, steps, flush, split, kernel, prefetch=0, warps=0, fused=True, graph=False,
-                  kv="bf16"):
+def measure_extra(name, device, steps, flush, split, kernel, fused=True, graph=False, kv="bf16"):
     w = inputs.make(name)
-    st = DecodeStep(w, device, split, kernel, prefetch, warps, fused, kv)
+    st = DecodeStep(w, device, split, kernel, fused, kv)
     total, attend = time_steps(st, steps, 3, flush, graph)
     att, _ = step_bytes(w, fused, kv)
     us = statistics.mean(attend) * 1e3
@@ -663,8 +653,7 @@ def run_native(args):
 
     _lib.load()  # fails loudly if the library is missing
     w = rank_workload(args.workload, rank)
-    step = DecodeStep(w, device, args.split_tokens, args.kernel, args.prefetch, args.warps,
-                      fused=not args.unfused, kv=args.kv)
+    step = DecodeStep(w, device, args.split_tokens, args.kernel, fused=not args.unfused, kv=args.kv)
     flush = make_l2_flush(device)
 
     att, write = step_bytes(w, step.fused, args.kv)
@@ -695,14 +684,14 @@ def run_native(args):
         for name in ("c2", "c3", "c5"):
             if name != args.workload:
                 extra[name] = measure_extra(name, device, 20, flush, args.split_tokens, args.kernel,
-                                            args.prefetch, args.warps, not args.unfused, args.graph)
+                                            not args.unfused, args.graph)
         if args.buckets:
             extra["graph_buckets_c2"] = measure_graph_buckets(device, flush)
         extra.update(measure_prefill(device, flush))
         # The int8 pool (the next row of the scope): the same workloads with
         # dequantisation fused into the attention kernel.
         for name in ("c4", "c3", "c5"):
-            extra[name + "_int8"] = measure_extra(name, device, 20, flush, args.split_tokens, "auto", 0, 0,
+            extra[name + "_int8"] = measure_extra(name, device, 20, flush, args.split_tokens, "auto",
                                                   not args.unfused, args.graph, kv="int8")
 
     cpu = cpu_baseline(w, args.cpu_seconds, args.kv) if rank == 0 else None
@@ -738,8 +727,6 @@ def run_native(args):
                 "kernel": args.kernel,
                 "kv": args.kv,
                 "launch": "CUDA graph replay of the step" if args.graph else "direct launches",
-                **({"prefetch": args.prefetch or 1, "warps_per_split": args.warps or 4}
-                   if args.kernel == "mma_ldg" else {}),
                 "step": ("pa_cache_write (one new token per sequence) + pa_decode" if not step.fused
                          else "pa_verify with one query per sequence: fused append of the new token "
                               "+ decode, one launch" if s.num_queries == 1
@@ -752,7 +739,6 @@ def run_native(args):
                 "bound": "hbm",
                 "kernel": ("pa_decode (attn_q8_kernel)" if args.kv == "int8" else
                            {"auto": "pa_decode (attn_mma_kernel)", "mma": "pa_decode (attn_mma_kernel)",
-                            "mma_ldg": "pa_decode (attn_ldg_kernel)",
                             "simt": "pa_decode (attn_simt_kernel)"}[args.kernel]),
                 "achieved": round(achieved, 1),
                 "peak": peak,
@@ -875,57 +861,12 @@ def run_prefill_only(args):
                       "dtype": "bf16", "data": "synthetic", "per_config": res}), flush=True)
 
 
-def run_floor(args):
-    """One JSON line: medians (us) of what the bench's CUDA events measure
-    around nothing, around one-element torch kernels, around one to three
-    back-to-back c3 decode steps, and around the c3 step with all lengths set
-    to 16 or to 384 tokens. Each timed region follows the same L2 flush and
-    device-side hold as the bench's own steps."""
-    import torch
-
-    device = torch.device("cuda", 0)
-    torch.cuda.set_device(device)
-    flush = make_l2_flush(device)
-    x = torch.zeros(1, device=device)
-    n = max(10, args.steps)
-
-    def median_us(fn):
-        for _ in range(3):
-            flush()
-            fn()
-        torch.cuda.synchronize()
-        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(n)]
-        for k in range(n):
-            flush()
-            gpu_hold()
-            ev[k][0].record()
-            fn()
-            ev[k][1].record()
-        torch.cuda.synchronize()
-        return round(statistics.median(e[0].elapsed_time(e[1]) * 1e3 for e in ev), 2)
-
-    res = {"empty_event_pair": median_us(lambda: None),
-           "one_element_kernel_x1": median_us(lambda: x.add_(1)),
-           "one_element_kernel_x10": median_us(lambda: [x.add_(1) for _ in range(10)])}
-    for name, kw in (("c3", {}), ("c3_len16", {"context_lens": (16,) * 64, "len_range": (0, 0)}),
-                     ("c3_len384", {"context_lens": (384,) * 64, "len_range": (0, 0)})):
-        st = DecodeStep(inputs.make("c3", **kw), device)
-        res[name + "_x1"] = median_us(st.attend)
-        if name == "c3":
-            res[name + "_x2"] = median_us(lambda: (st.attend(), st.attend()))
-            res[name + "_x3"] = median_us(lambda: (st.attend(), st.attend(), st.attend()))
-    print(json.dumps({"metric": "fixed cost of one call under the bench's CUDA events", "unit": "us",
-                      "steps": n, "data": "synthetic", "per_config": res}), flush=True)
-
-
 def main():
     args = parse_args()
     if args.record_traffic:
         print(json.dumps(record_traffic(*args.record_traffic)))
     elif args.prefill:
         run_prefill_only(args)
-    elif args.floor:
-        run_floor(args)
     elif args.impl == "reference":
         run_reference(args)
     else:

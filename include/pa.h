@@ -66,9 +66,11 @@
  *    block, channel), [kv_heads, num_blocks, head_dim]. v_scale holds one per
  *    (kv head, block, row), [kv_heads, num_blocks, block_size].
  *  - A stored value is (byte - 128) * scale.
- *  - Quantising a group takes s = max|x| / 127 and q = x / s rounded to
- *    nearest, ties to even, in fp32 with IEEE division. An all-zero group
- *    has s = 0 and bytes 128.
+ *  - Quantising a group with m = max|x| > 0 stores the scale s = m / 127
+ *    and the codes q = RN(x * (127 / m)), clamped to [-127, 127]: one IEEE
+ *    fp32 division per group (127 / m), then one fp32 multiply per element,
+ *    rounded to nearest with ties to even. An all-zero group has s = 0 and
+ *    bytes 128.
  *  - Queries, new rows and outputs are bf16. Attention dequantises inside
  *    the kernel. K values enter the products rounded to f16; V bytes enter
  *    exactly, with the row scales folded into the softmax weights. K values
@@ -128,14 +130,13 @@ typedef enum pa_kernel {
     PA_KERNEL_AUTO = 0,    /* bf16: PA_KERNEL_MMA; fp32: PA_KERNEL_SIMT */
     PA_KERNEL_MMA = 1,     /* bf16 only: a producer warp stages 16-token K/V tiles with TMA
                               tensor loads; bf16 tensor-core products, fp32 softmax */
-    PA_KERNEL_SIMT = 2,    /* CUDA-core fp32 arithmetic, any dtype (fp32 caches; comparison) */
-    PA_KERNEL_MMA_LDG = 3, /* bf16 only: as PA_KERNEL_MMA but each warp loads its own tiles with
-                              16-byte loads staged through shared memory (kept for comparison) */
+    PA_KERNEL_SIMT = 2,    /* CUDA-core fp32 arithmetic, any dtype (the fp32 caches' kernel) */
     PA_KERNEL_TC = 4       /* pa_prefill only (its default): tcgen05 products with the S and O
                               accumulators and the Q and P operands in tensor memory */
 } pa_kernel;
 
-/* Optional tuning for pa_decode / pa_verify; pass NULL for the defaults. */
+/* Optional settings for pa_decode / pa_verify / pa_verify_ragged /
+ * pa_prefill; pass NULL for the defaults. */
 typedef struct pa_options {
     /* Tokens per context split (flash-decoding split-K). A positive multiple
      * of block_size: every sequence uses this split. 0 = the default rule:
@@ -146,17 +147,17 @@ typedef struct pa_options {
      * batch-mates, so its result is bit-identical across batch compositions. */
     int32_t split_tokens;
     int32_t kernel;   /* pa_kernel */
-    /* PA_KERNEL_MMA_LDG only: 16-token blocks each warp keeps in flight, 1 or 2;
-     * 0 = default (PA_DEFAULT_PREFETCH). Values above 1 apply to up to 8 query
-     * rows per (sequence, KV head). */
-    int32_t prefetch;
-    /* PA_KERNEL_MMA_LDG only: warps that share one split, 1, 2 or 4; 0 = default
-     * (PA_DEFAULT_WARPS). */
-    int32_t warps;
+    /* Bound, in nanoseconds, on each wait of the tensor-core attention
+     * kernels for a shared-memory stage or a peer warp; 0 = the default,
+     * PA_DEFAULT_WAIT_LIMIT_NS (one second). A wait that runs past it raises
+     * PA_FLAG_TIMEOUT, and the CTA lets its own copies in flight land (under
+     * the default bound) and returns without writing its rows. The default
+     * is far above any wait of a healthy call; a small value exists to
+     * exercise the timeout path, whose results are then not valid. */
+    uint32_t wait_limit_ns;
 } pa_options;
 
-#define PA_DEFAULT_PREFETCH 1
-#define PA_DEFAULT_WARPS 4
+#define PA_DEFAULT_WAIT_LIMIT_NS 1000000000u
 
 #define PA_DEFAULT_SPLIT_TOKENS 1536
 #define PA_LONG_CONTEXT_TOKENS 4096
@@ -290,7 +291,7 @@ pa_status pa_verify(const pa_cache *cache, const void *d_q, void *d_out, const v
  *                  PA_FLAG_BAD_LENGTH.
  *   max_queries    host bound on every n_b (>= 1); the workspace is sized with
  *                  it as num_queries (pa_workspace_size).
- *   Other arguments as in pa_verify. PA_KERNEL_MMA_LDG is not supported here.
+ *   Other arguments as in pa_verify.
  */
 pa_status pa_verify_ragged(const pa_cache *cache, const void *d_q, void *d_out, const void *d_k_new,
                            const void *d_v_new, const int32_t *d_slot_mapping,
@@ -316,12 +317,14 @@ pa_status pa_verify_ragged(const pa_cache *cache, const void *d_q, void *d_out, 
  *                  max_queries bounds every n_b (it sizes the grid).
  *   d_workspace    optional (NULL: no status word): a 256-byte-aligned buffer of
  *                  >= 256 bytes whose first word receives PA_FLAG_* bits.
- *   opts           optional; only opts->kernel is read: PA_KERNEL_AUTO or
- *                  PA_KERNEL_TC (tcgen05 kernel, two CTAs per SM; needs
- *                  q_heads / kv_heads <= 128, else PA_ERR_UNSUPPORTED) or
- *                  PA_KERNEL_MMA (warp-level mma.sync kernel, kept for
- *                  comparison); anything else returns PA_ERR_UNSUPPORTED.
- *                  AUTO takes the tcgen05 kernel when the group allows it.
+ *   opts           optional; opts->kernel and opts->wait_limit_ns are read
+ *                  (split_tokens is not: a prefill has no split). kernel is
+ *                  PA_KERNEL_AUTO, PA_KERNEL_TC (tcgen05 kernel, two CTAs per
+ *                  SM; needs q_heads / kv_heads <= 128, else
+ *                  PA_ERR_UNSUPPORTED) or PA_KERNEL_MMA (warp-level mma.sync
+ *                  kernel: the one AUTO takes for groups above 128, where a
+ *                  tcgen05 row tile cannot hold whole tokens); anything else
+ *                  returns PA_ERR_UNSUPPORTED.
  *   Other arguments as in pa_decode. No split-K: one CTA reads the whole
  *   visible context of its 128 rows.
  */
@@ -358,14 +361,21 @@ pa_status pa_validate(const pa_cache *cache, const int32_t *d_block_tables,
  *
  * Arguments and results are those of pa_decode without the workspace: the
  * split partials, arrival counters and status word live instead in one
- * library-owned device array of PA_NOALLOC_SCRATCH_BYTES, which every GPU that
- * loads the library holds until the process exits. The call itself allocates
- * and frees nothing.
- *  - Sizes whose pa_workspace_size() exceeds PA_NOALLOC_SCRATCH_BYTES return
+ * library-owned device array of PA_NOALLOC_SCRATCH_BYTES.
+ *  - The first call on a device sets the array up there: it looks up the
+ *    array's address with that device current, and that lookup loads the
+ *    library's code module holding the array, so the CUDA runtime places the
+ *    array (PA_NOALLOC_SCRATCH_BYTES of device memory) on the device at that
+ *    moment (under the runtime's default lazy module loading; with
+ *    CUDA_MODULE_LOADING=EAGER it is placed when the device's context is
+ *    created). The device then holds it until the process exits. Make that
+ *    first call at start-up: before the footprint must stay fixed and before
+ *    any stream capture on the device. Every later call allocates and frees
+ *    nothing.
+ *  - Arguments are checked as pa_decode checks them, before anything else; a
+ *    rejected call returns pa_decode's status and touches nothing. Sizes
+ *    whose pa_workspace_size() exceeds PA_NOALLOC_SCRATCH_BYTES then return
  *    PA_ERR_WORKSPACE before anything is launched.
- *  - The first call on a device looks up that device's address of the array
- *    (with that device current); make that first call before any stream
- *    capture on the device.
  *  - Every call reuses the same array and clears the parts that must start at
  *    zero. Calls whose work overlaps on the GPU (different streams, or
  *    different host threads on one device) race on it: serialise them.

@@ -24,10 +24,8 @@ PA_DTYPE_INT8 = 2
 PA_KERNEL_AUTO = 0
 PA_KERNEL_MMA = 1
 PA_KERNEL_SIMT = 2
-PA_KERNEL_MMA_LDG = 3
 PA_KERNEL_TC = 4
-PA_DEFAULT_PREFETCH = 1
-PA_DEFAULT_WARPS = 4
+PA_DEFAULT_WAIT_LIMIT_NS = 1000000000
 
 PA_FLAG_BAD_BLOCK = 0x1
 PA_FLAG_BAD_LENGTH = 0x2
@@ -57,7 +55,7 @@ class PaCache(ctypes.Structure):
 
 class PaOptions(ctypes.Structure):
     _fields_ = [("split_tokens", ctypes.c_int32), ("kernel", ctypes.c_int32),
-                ("prefetch", ctypes.c_int32), ("warps", ctypes.c_int32)]
+                ("wait_limit_ns", ctypes.c_uint32)]
 
 
 class PaError(RuntimeError):

@@ -17,8 +17,7 @@ import torch
 from . import _lib as L
 
 _DTYPES = {torch.bfloat16: L.PA_DTYPE_BF16, torch.float32: L.PA_DTYPE_F32, torch.uint8: L.PA_DTYPE_INT8}
-_KERNELS = {"auto": L.PA_KERNEL_AUTO, "mma": L.PA_KERNEL_MMA, "simt": L.PA_KERNEL_SIMT,
-            "mma_ldg": L.PA_KERNEL_MMA_LDG, "tc": L.PA_KERNEL_TC}
+_KERNELS = {"auto": L.PA_KERNEL_AUTO, "mma": L.PA_KERNEL_MMA, "simt": L.PA_KERNEL_SIMT, "tc": L.PA_KERNEL_TC}
 
 
 def _vp(t: Optional[torch.Tensor]):
@@ -76,9 +75,9 @@ def _row_dtype(k_cache: torch.Tensor):
 
 
 @functools.lru_cache(maxsize=64)
-def _options(split_tokens: int, kernel: str, prefetch: int = 0, warps: int = 0) -> L.PaOptions:
+def _options(split_tokens: int, kernel: str, wait_limit_ns: int = 0) -> L.PaOptions:
     """Options struct for these values (cached: libpa only reads it)."""
-    return L.PaOptions(int(split_tokens), _KERNELS[kernel], int(prefetch), int(warps))
+    return L.PaOptions(int(split_tokens), _KERNELS[kernel], int(wait_limit_ns))
 
 
 def pa_workspace_size(batch: int, num_queries: int, q_heads: int, kv_heads: int,
@@ -139,8 +138,11 @@ def _tables(block_tables, context_lens, batch):
 
 def pa_decode(k_cache, v_cache, q, block_tables, context_lens, max_context_len: int, scale: float,
               workspace, out=None, split_tokens: int = 0, kernel: str = "auto", stream=None,
-              prefetch: int = 0, warps: int = 0, k_scale=None, v_scale=None):
-    """out[b, hq] = softmax(scale * q[b, hq] . K_b^T) V_b over sequence b's paged context."""
+              k_scale=None, v_scale=None, wait_limit_ns: int = 0):
+    """out[b, hq] = softmax(scale * q[b, hq] . K_b^T) V_b over sequence b's paged context.
+
+    wait_limit_ns: bound on each device-side pipeline wait (0: one second);
+    a wait past it raises PA_FLAG_TIMEOUT in the workspace status word."""
     cache = make_cache(k_cache, v_cache, k_scale, v_scale)
     _need(q.dim() == 3 and q.dtype == _row_dtype(k_cache) and q.is_contiguous(),
           "q must be [batch, q_heads, head_dim] of the row dtype")
@@ -148,7 +150,7 @@ def pa_decode(k_cache, v_cache, q, block_tables, context_lens, max_context_len: 
     mbps = _tables(block_tables, context_lens, batch)
     if out is None:
         out = torch.empty_like(q)
-    opts = _options(split_tokens, kernel, prefetch, warps)
+    opts = _options(split_tokens, kernel, wait_limit_ns)
     L.check("pa_decode", L.load().pa_decode(
         ctypes.byref(cache), _vp(q), _vp(out), _vp(block_tables), mbps, _vp(context_lens), batch,
         q_heads, int(max_context_len), float(scale), _vp(workspace),
@@ -181,8 +183,7 @@ def pa_decode_noalloc(k_cache, v_cache, q, block_tables, context_lens, max_conte
 
 def pa_verify(k_cache, v_cache, q, k_new, v_new, slot_mapping, block_tables, context_lens,
               max_context_len: int, scale: float, workspace, out=None, split_tokens: int = 0,
-              kernel: str = "auto", stream=None, prefetch: int = 0, warps: int = 0, k_scale=None,
-              v_scale=None):
+              kernel: str = "auto", stream=None, k_scale=None, v_scale=None, wait_limit_ns: int = 0):
     """Fused speculative verify: write the new K/V, attend causally. q: [batch, nq, q_heads, head_dim]."""
     cache = make_cache(k_cache, v_cache, k_scale, v_scale)
     _need(q.dim() == 4 and q.dtype == _row_dtype(k_cache) and q.is_contiguous(),
@@ -196,7 +197,7 @@ def pa_verify(k_cache, v_cache, q, k_new, v_new, slot_mapping, block_tables, con
           "new rows must be [batch * num_queries, kv_heads, head_dim] of the cache dtype")
     if out is None:
         out = torch.empty_like(q)
-    opts = _options(split_tokens, kernel, prefetch, warps)
+    opts = _options(split_tokens, kernel, wait_limit_ns)
     L.check("pa_verify", L.load().pa_verify(
         ctypes.byref(cache), _vp(q), _vp(out), _vp(k_new), _vp(v_new), _vp(slot_mapping), nq,
         _vp(block_tables), mbps, _vp(context_lens), batch, q_heads, int(max_context_len),
@@ -208,7 +209,7 @@ def pa_verify(k_cache, v_cache, q, k_new, v_new, slot_mapping, block_tables, con
 def pa_verify_ragged(k_cache, v_cache, q, k_new, v_new, slot_mapping, query_start, block_tables,
                      context_lens, max_context_len: int, scale: float, workspace, max_queries: int,
                      out=None, split_tokens: int = 0, kernel: str = "auto", stream=None, k_scale=None,
-                     v_scale=None):
+                     v_scale=None, wait_limit_ns: int = 0):
     """Verify with a different number of new tokens per sequence, in one launch.
 
     q: [total, q_heads, head_dim]; sequence b owns rows query_start[b] ..
@@ -229,7 +230,7 @@ def pa_verify_ragged(k_cache, v_cache, q, k_new, v_new, slot_mapping, query_star
           "new rows must be [total_queries, kv_heads, head_dim] of the row dtype")
     if out is None:
         out = torch.empty_like(q)
-    opts = _options(split_tokens, kernel)
+    opts = _options(split_tokens, kernel, wait_limit_ns)
     L.check("pa_verify_ragged", L.load().pa_verify_ragged(
         ctypes.byref(cache), _vp(q), _vp(out), _vp(k_new), _vp(v_new), _vp(slot_mapping), _vp(query_start),
         total, int(max_queries), _vp(block_tables), mbps, _vp(context_lens), batch, q_heads,
@@ -239,7 +240,8 @@ def pa_verify_ragged(k_cache, v_cache, q, k_new, v_new, slot_mapping, query_star
 
 
 def pa_prefill(k_cache, v_cache, q, query_start, block_tables, context_lens, max_context_len: int,
-               scale: float, max_queries: int, out=None, workspace=None, stream=None, kernel: str = "auto"):
+               scale: float, max_queries: int, out=None, workspace=None, stream=None, kernel: str = "auto",
+               wait_limit_ns: int = 0):
     """Causal attention of each sequence's prompt chunk (its last n_b positions,
     already in the cache) over its paged context. q: [total, q_heads, head_dim]
     bf16; query_start: int32 [batch + 1]. workspace (optional) receives the
@@ -258,7 +260,7 @@ def pa_prefill(k_cache, v_cache, q, query_start, block_tables, context_lens, max
     L.check("pa_prefill", L.load().pa_prefill(
         ctypes.byref(cache), _vp(q), _vp(out), _vp(query_start), total, int(max_queries), _vp(block_tables),
         mbps, _vp(context_lens), batch, q_heads, int(max_context_len), float(scale), _vp(workspace), ws_bytes,
-        ctypes.byref(_options(0, kernel)), _stream(stream)))
+        ctypes.byref(_options(0, kernel, wait_limit_ns)), _stream(stream)))
     return out
 
 

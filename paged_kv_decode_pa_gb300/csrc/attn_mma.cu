@@ -165,7 +165,7 @@ __global__ void __launch_bounds__(kMmaThreads, NT == 1 ? 4 : 3)
     // context are zeroed. Then the stage's full barrier completes.
     auto patch_next = [&]() -> bool {
       const int k = patched, s = k % kStages;
-      if (!__all_sync(0xffffffffu, mbar_wait(bar_land + 8 * s, ((k - jf) / kStages) & 1))) return false;
+      if (!__all_sync(0xffffffffu, mbar_wait(bar_land + 8 * s, ((k - jf) / kStages) & 1, p.wait_limit_ns))) return false;
       uint8_t* kt_ptr = sbase + MmaSmem::stages + s * kStageBytes;
       uint8_t* vt_ptr = kt_ptr + kTileBytes;
       const int tok0 = w.t0 + k * kBlockSize;
@@ -213,7 +213,7 @@ __global__ void __launch_bounds__(kMmaThreads, NT == 1 ? 4 : 3)
     const uint64_t policy = policy_evict_first();
     auto issue = [&](int j) -> bool {  // lane 0
       const int s = j % kStages, n = j / kStages;
-      if (n > 0 && !mbar_wait(bar_empty + 8 * s, (n - 1) & 1)) return false;
+      if (n > 0 && !mbar_wait(bar_empty + 8 * s, (n - 1) & 1, p.wait_limit_ns)) return false;
       const uint32_t st = base + MmaSmem::stages + s * kStageBytes;
       const uint32_t fb = (j >= jf ? bar_land : bar_full) + 8 * s;
       int id = s_ids[j];
@@ -285,7 +285,7 @@ __global__ void __launch_bounds__(kMmaThreads, NT == 1 ? 4 : 3)
 
     for (int j = warp; j < nblk; j += kMmaConsumers) {
       const int s = j % kStages;
-      if (!mbar_wait(bar_full + 8 * s, (j / kStages) & 1)) {
+      if (!mbar_wait(bar_full + 8 * s, (j / kStages) & 1, p.wait_limit_ns)) {
         raise_flag(p.status, PA_FLAG_TIMEOUT);
         s_flag[2] = 1;
         break;
@@ -375,16 +375,11 @@ size_t mma_smem_bytes() { return MmaSmem::alloc; }
 template <int NT>
 static cudaError_t launch_nt(const CUtensorMap& tk, const CUtensorMap& tv, const AttnParams& p,
                              dim3 grid, cudaStream_t stream) {
-  static int configured[64] = {0};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev >= 0 && dev < 64 && !configured[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(attn_mma_kernel<NT>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         MmaSmem::alloc);
-    if (e != cudaSuccess) return e;
-    configured[dev] = 1;
-  }
+  static PerDeviceOnce once;
+  const cudaError_t e = once.run([](int) {
+    return cudaFuncSetAttribute(attn_mma_kernel<NT>, cudaFuncAttributeMaxDynamicSharedMemorySize, MmaSmem::alloc);
+  });
+  if (e != cudaSuccess) return e;
   attn_mma_kernel<NT><<<grid, kMmaThreads, MmaSmem::alloc, stream>>>(tk, tv, p);
   return cudaGetLastError();
 }

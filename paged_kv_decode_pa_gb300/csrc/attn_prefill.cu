@@ -105,7 +105,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         int id = __shfl_sync(0xffffffffu, ids, k);
         if (lane == 0) {
           const int s = j % kPfStages, ph = j / kPfStages;
-          if (ph > 0 && !mbar_wait(bar_empty + 8 * s, (ph - 1) & 1)) {
+          if (ph > 0 && !mbar_wait(bar_empty + 8 * s, (ph - 1) & 1, p.wait_limit_ns)) {
             timed_out = true;
           } else {
             if (id < 0 || id >= p.num_blocks) {
@@ -132,7 +132,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     if (!timed_out && nblk > 0) {
       const int j = nblk - 1, s = j % kPfStages;
       if (tail_valid < kBlockSize) {
-        if (__all_sync(0xffffffffu, mbar_wait(bar_full + 8 * s, (j / kPfStages) & 1))) {
+        if (__all_sync(0xffffffffu, mbar_wait(bar_full + 8 * s, (j / kPfStages) & 1, p.wait_limit_ns))) {
           uint8_t* vt = sbase + PfSmem::stages + s * kBlockBytes + kTileBytes;
           for (int e = lane; e < (kBlockSize - tail_valid) * 16; e += 32) {
             const int t = tail_valid + (e >> 4), ch = e & 15;
@@ -179,8 +179,8 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     const int wlast = wrows > 0 ? row_limit(p, L, nq, wrow0 + wrows - 1) : -1;
     for (int j = 0; j < nblk; ++j) {
       const int s = j % kPfStages;
-      if (!mbar_wait(bar_full + 8 * s, (j / kPfStages) & 1) ||
-          (j == nblk - 1 && !mbar_wait(bar_tail, 0))) {
+      if (!mbar_wait(bar_full + 8 * s, (j / kPfStages) & 1, p.wait_limit_ns) ||
+          (j == nblk - 1 && !mbar_wait(bar_tail, 0, p.wait_limit_ns))) {
         timed_out = true;
         break;
       }
@@ -228,15 +228,11 @@ __global__ void __launch_bounds__(kPfThreads, 1)
 
 cudaError_t launch_attn_prefill(const CUtensorMap& tk, const CUtensorMap& tv, const AttnParams& p, dim3 grid,
                                 cudaStream_t stream) {
-  static int configured[64] = {0};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev >= 0 && dev < 64 && !configured[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(attn_prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         PfSmem::alloc);
-    if (e != cudaSuccess) return e;
-    configured[dev] = 1;
-  }
+  static PerDeviceOnce once;
+  const cudaError_t e = once.run([](int) {
+    return cudaFuncSetAttribute(attn_prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, PfSmem::alloc);
+  });
+  if (e != cudaSuccess) return e;
   attn_prefill_kernel<<<grid, kPfThreads, PfSmem::alloc, stream>>>(tk, tv, p);
   return cudaGetLastError();
 }

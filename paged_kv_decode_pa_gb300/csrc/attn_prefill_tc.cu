@@ -182,6 +182,7 @@ __global__ void __launch_bounds__(kTcThreads, kTcCtasPerSm)
     const uint64_t policy = policy_evict_last();  // other row tiles re-read the same context
     bool failed = false;
     int g = 0, nitem = 0;  // context steps issued and items with steps so far
+    int k_ahead = 0;       // lane 0: 1 while step g's K is issued but its V is not
     for (int k = 0; !failed; ++k) {
       const int pos = tc_item_pos(k);
       if (pos >= items) break;
@@ -189,7 +190,7 @@ __global__ void __launch_bounds__(kTcThreads, kTcCtasPerSm)
       if (w.ntile == 0) continue;
       if (lane == 0) {
         // Q of this item, once every S of the previous one has completed.
-        if (*abort_flag || (nitem > 0 && !mbar_wait(b_qfree, (nitem - 1) & 1))) {
+        if (*abort_flag || (nitem > 0 && !mbar_wait(b_qfree, (nitem - 1) & 1, p.wait_limit_ns))) {
           failed = true;
         } else {
           const int z = w.q0 + w.row0 / p.group;
@@ -224,9 +225,10 @@ __global__ void __launch_bounds__(kTcThreads, kTcCtasPerSm)
             y[i] = (real && id[i] >= 0 && id[i] < p.num_blocks) ? id[i] * kBlockSize : -kBlockSize;
           }
           // K once the stage's S has completed, V once its P.V has.
-          if (*abort_flag || (ph > 0 && !mbar_wait(bk_empty + 8 * s, (ph - 1) & 1))) {
+          if (*abort_flag || (ph > 0 && !mbar_wait(bk_empty + 8 * s, (ph - 1) & 1, p.wait_limit_ns))) {
             failed = true;
           } else {
+            k_ahead = 1;  // this step's K is in flight until its V is issued too
             const uint32_t kd = base + TcSmem::k + s * kTcTileBytes, kb = bk_full + 8 * s;
             mbar_arrive_expect_tx(kb, kTcTileBytes);
 #pragma unroll
@@ -235,7 +237,7 @@ __global__ void __launch_bounds__(kTcThreads, kTcCtasPerSm)
               tma_load_3d(kd + kTcHalf + i * kBlockSize * 128, &tmap_k, 64, y[i], w.h, kb, policy);
             }
           }
-          if (!failed && ph > 0 && !mbar_wait(bv_empty + 8 * s, (ph - 1) & 1)) failed = true;
+          if (!failed && ph > 0 && !mbar_wait(bv_empty + 8 * s, (ph - 1) & 1, p.wait_limit_ns)) failed = true;
           if (!failed) {
             const uint32_t vd = base + TcSmem::v + s * kTcTileBytes, vb = bv_full + 8 * s;
             mbar_arrive_expect_tx(vb, kTcTileBytes);
@@ -244,6 +246,7 @@ __global__ void __launch_bounds__(kTcThreads, kTcCtasPerSm)
               tma_load_3d(vd + i * kBlockSize * 128, &tmap_v, 0, y[i], w.h, vb, policy);
               tma_load_3d(vd + kTcHalf + i * kBlockSize * 128, &tmap_v, 64, y[i], w.h, vb, policy);
             }
+            k_ahead = 0;
           }
         }
         failed = __shfl_sync(0xffffffffu, failed, 0);
@@ -254,10 +257,10 @@ __global__ void __launch_bounds__(kTcThreads, kTcCtasPerSm)
       raise_flag(p.status, PA_FLAG_TIMEOUT);
       *abort_flag = 1;
       // Let the loads already issued land (bounded) before the CTA can leave.
-      for (int gg = max(0, g - kTcStages); gg < g; ++gg) {
+      for (int gg = max(0, g + k_ahead - kTcStages); gg < g + k_ahead; ++gg) {
         const int s = gg % kTcStages, par = (gg / kTcStages) & 1;
         (void)mbar_wait(bk_full + 8 * s, par);
-        (void)mbar_wait(bv_full + 8 * s, par);
+        if (gg < g) (void)mbar_wait(bv_full + 8 * s, par);
       }
       if (nitem > 0) (void)mbar_wait(b_qfull, (nitem - 1) & 1);
     }
@@ -303,7 +306,7 @@ __global__ void __launch_bounds__(kTcThreads, kTcCtasPerSm)
       ++k;
       int g = 0, nitem = 0;
       if (have) {
-        ok = mbar_wait(b_qfull, 0) && mbar_wait(bk_full, 0);
+        ok = mbar_wait(b_qfull, 0, p.wait_limit_ns) && mbar_wait(bk_full, 0, p.wait_limit_ns);
         if (ok) {
           tc_fence_after_sync();
           issue_s(0);
@@ -317,8 +320,8 @@ __global__ void __launch_bounds__(kTcThreads, kTcCtasPerSm)
           const bool more = j + 1 < cur.ntile;
           if (more || have_nxt) {
             const int g1 = gg + 1, s1 = g1 % kTcStages, par1 = (g1 / kTcStages) & 1;
-            if (*abort_flag || !mbar_wait(b_sfree, gg & 1) || !mbar_wait(bk_full + 8 * s1, par1) ||
-                (!more && !mbar_wait(b_qfull, (nitem + 1) & 1))) {
+            if (*abort_flag || !mbar_wait(b_sfree, gg & 1, p.wait_limit_ns) || !mbar_wait(bk_full + 8 * s1, par1, p.wait_limit_ns) ||
+                (!more && !mbar_wait(b_qfull, (nitem + 1) & 1, p.wait_limit_ns))) {
               ok = false;
               break;
             }
@@ -329,8 +332,8 @@ __global__ void __launch_bounds__(kTcThreads, kTcCtasPerSm)
           }
           // P.V of this step; an item's first P.V overwrites O, once the
           // softmax has read the previous item's.
-          if (!mbar_wait(b_pfull, gg & 1) || !mbar_wait(bv_full + 8 * s, par) ||
-              (j == 0 && nitem > 0 && !mbar_wait(b_ofree, (nitem - 1) & 1))) {
+          if (!mbar_wait(b_pfull, gg & 1, p.wait_limit_ns) || !mbar_wait(bv_full + 8 * s, par, p.wait_limit_ns) ||
+              (j == 0 && nitem > 0 && !mbar_wait(b_ofree, (nitem - 1) & 1, p.wait_limit_ns))) {
             ok = false;
             break;
           }
@@ -390,7 +393,7 @@ __global__ void __launch_bounds__(kTcThreads, kTcCtasPerSm)
       float m = -INFINITY, l = 0.f;
       for (int j = 0; j < w.ntile; ++j) {
         const int gg = g + j;
-        if (__any_sync(0xffffffffu, *abort_flag != 0) || !__all_sync(0xffffffffu, mbar_wait(b_sfull, gg & 1))) {
+        if (__any_sync(0xffffffffu, *abort_flag != 0) || !__all_sync(0xffffffffu, mbar_wait(b_sfull, gg & 1, p.wait_limit_ns))) {
           ok = false;
           break;
         }
@@ -446,7 +449,7 @@ __global__ void __launch_bounds__(kTcThreads, kTcCtasPerSm)
             m = m_new;
           }
           if (j > 0) {
-            if (!__all_sync(0xffffffffu, mbar_wait(b_odone, (gg - 1) & 1))) {
+            if (!__all_sync(0xffffffffu, mbar_wait(b_odone, (gg - 1) & 1, p.wait_limit_ns))) {
               ok = false;
               break;
             }
@@ -489,7 +492,7 @@ __global__ void __launch_bounds__(kTcThreads, kTcCtasPerSm)
         }
         l += sum;
         if (!pv_done) {
-          if (!__all_sync(0xffffffffu, mbar_wait(b_odone, (gg - 1) & 1))) {
+          if (!__all_sync(0xffffffffu, mbar_wait(b_odone, (gg - 1) & 1, p.wait_limit_ns))) {
             ok = false;
             break;
           }
@@ -499,7 +502,7 @@ __global__ void __launch_bounds__(kTcThreads, kTcCtasPerSm)
           // The item's last block: zero its V rows past the context once they
           // have landed, before P hands the stage to the product.
           const int s = gg % kTcStages;
-          if (!__all_sync(0xffffffffu, mbar_wait(bv_full + 8 * s, (gg / kTcStages) & 1))) {
+          if (!__all_sync(0xffffffffu, mbar_wait(bv_full + 8 * s, (gg / kTcStages) & 1, p.wait_limit_ns))) {
             ok = false;
             break;
           }
@@ -520,7 +523,7 @@ __global__ void __launch_bounds__(kTcThreads, kTcCtasPerSm)
       if (!ok) break;
       g += w.ntile;
       // The item's output: O after its last P.V, read out, handed back, then stored.
-      if (!__all_sync(0xffffffffu, mbar_wait(b_odone, (g - 1) & 1))) {
+      if (!__all_sync(0xffffffffu, mbar_wait(b_odone, (g - 1) & 1, p.wait_limit_ns))) {
         ok = false;
         break;
       }
@@ -569,18 +572,17 @@ __global__ void __launch_bounds__(kTcThreads, kTcCtasPerSm)
 
 cudaError_t launch_attn_prefill_tc(const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tq,
                                    const AttnParams& p, cudaStream_t stream) {
-  static int configured[64] = {0};
-  static int sms[64] = {0};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  if (!configured[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(attn_prefill_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  static PerDeviceOnce once;
+  static int sms[kMaxDevices] = {0};
+  const cudaError_t e = once.run([](int dev) {
+    cudaError_t r = cudaFuncSetAttribute(attn_prefill_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          TcSmem::alloc);
-    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms[dev], cudaDevAttrMultiProcessorCount, dev);
-    if (e != cudaSuccess) return e;
-    configured[dev] = 1;
-  }
+    if (r == cudaSuccess) r = cudaDeviceGetAttribute(&sms[dev], cudaDevAttrMultiProcessorCount, dev);
+    return r;
+  });
+  if (e != cudaSuccess) return e;
+  int dev = 0;
+  cudaGetDevice(&dev);  // in range: run() checked it
   const int64_t items = int64_t(p.row_groups) * p.kv_heads * p.batch;
   const int64_t slots = int64_t(kTcCtasPerSm) * sms[dev];
   const unsigned grid = unsigned(items < slots ? items : slots);

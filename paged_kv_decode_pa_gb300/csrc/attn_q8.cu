@@ -274,7 +274,7 @@ __global__ void __launch_bounds__(kQ8Threads, NT == 1 ? 5 : 3)
       int issued = 0;
       for (int j = 0; j < nblk; ++j) {
         const int s = j % kQ8Stages, n = j / kQ8Stages;
-        if (n > 0 && !mbar_wait(bar_empty + 8 * s, (n - 1) & 1)) {
+        if (n > 0 && !mbar_wait(bar_empty + 8 * s, (n - 1) & 1, p.wait_limit_ns)) {
           raise_flag(p.status, PA_FLAG_TIMEOUT);
           s_flag[2] = 1;
           break;
@@ -305,7 +305,7 @@ __global__ void __launch_bounds__(kQ8Threads, NT == 1 ? 5 : 3)
         const int s = j % kQ8Stages;
         // Every lane waits (each then sees the landed bytes); the warp goes on
         // only if all of them saw the phase complete.
-        if (!__all_sync(0xffffffffu, mbar_wait(bar_full + 8 * s, (j / kQ8Stages) & 1))) {
+        if (!__all_sync(0xffffffffu, mbar_wait(bar_full + 8 * s, (j / kQ8Stages) & 1, p.wait_limit_ns))) {
           if (lane == 0) {
             raise_flag(p.status, PA_FLAG_TIMEOUT);
             s_flag[2] = 1;
@@ -353,8 +353,8 @@ __global__ void __launch_bounds__(kQ8Threads, NT == 1 ? 5 : 3)
       const int j0 = 2 * pi;
       const bool two = j0 + 1 < nmain;
       const int s0 = j0 % kQ8Stages, s1 = (j0 + 1) % kQ8Stages;
-      if (!mbar_wait(bar_full + 8 * s0, (j0 / kQ8Stages) & 1) ||
-          (two && !mbar_wait(bar_full + 8 * s1, ((j0 + 1) / kQ8Stages) & 1))) {
+      if (!mbar_wait(bar_full + 8 * s0, (j0 / kQ8Stages) & 1, p.wait_limit_ns) ||
+          (two && !mbar_wait(bar_full + 8 * s1, ((j0 + 1) / kQ8Stages) & 1, p.wait_limit_ns))) {
         timed_out = true;
         break;
       }
@@ -384,11 +384,11 @@ __global__ void __launch_bounds__(kQ8Threads, NT == 1 ? 5 : 3)
     for (int j = nmain; j < nblk && !timed_out; ++j) {
       if ((j >> 1) % kQ8Consumers != warp) continue;
       const int s0 = j % kQ8Stages;
-      if (!mbar_wait(bar_full + 8 * s0, (j / kQ8Stages) & 1)) {
+      if (!mbar_wait(bar_full + 8 * s0, (j / kQ8Stages) & 1, p.wait_limit_ns)) {
         timed_out = true;
         break;
       }
-      if (!mbar_wait(bar_fixed + 8 * (j - nmain), 0)) {
+      if (!mbar_wait(bar_fixed + 8 * (j - nmain), 0, p.wait_limit_ns)) {
         timed_out = true;
         break;
       }
@@ -451,15 +451,11 @@ __global__ void __launch_bounds__(kQ8Threads, NT == 1 ? 5 : 3)
 template <int NT>
 static cudaError_t launch_q8_nt(const Q8Maps& maps, const AttnParams& p, dim3 grid, bool after_append,
                                 cudaStream_t stream) {
-  static int configured[64] = {0};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev >= 0 && dev < 64 && !configured[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(attn_q8_kernel<NT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         Q8Smem::alloc);
-    if (e != cudaSuccess) return e;
-    configured[dev] = 1;
-  }
+  static PerDeviceOnce once;
+  const cudaError_t e = once.run([](int) {
+    return cudaFuncSetAttribute(attn_q8_kernel<NT>, cudaFuncAttributeMaxDynamicSharedMemorySize, Q8Smem::alloc);
+  });
+  if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = dim3(kQ8Threads, 1, 1);

@@ -14,7 +14,6 @@ namespace pa {
 cudaError_t launch_attn_mma(const CUtensorMap& tk, const CUtensorMap& tv, const AttnParams& p,
                             dim3 grid, cudaStream_t stream);
 cudaError_t launch_attn_simt(const AttnParams& p, bool bf16, dim3 grid, cudaStream_t stream);
-cudaError_t launch_attn_ldg(const AttnParams& p, int prefetch, int warps, cudaStream_t stream);
 cudaError_t launch_merge(const AttnParams& p, cudaStream_t stream);
 struct Q8Maps {
   CUtensorMap k, v, ks, vs;
@@ -63,6 +62,10 @@ pa_status check_cache(const pa_cache* c) {
 
 int32_t split_of(const pa_options* o) {
   return (o && o->split_tokens > 0) ? o->split_tokens : PA_DEFAULT_SPLIT_TOKENS;
+}
+
+uint32_t wait_limit_of(const pa_options* o) {
+  return (o && o->wait_limit_ns > 0) ? o->wait_limit_ns : PA_DEFAULT_WAIT_LIMIT_NS;
 }
 
 // Split for sequences longer than PA_LONG_CONTEXT_TOKENS under the default
@@ -259,6 +262,35 @@ __global__ void validate_kernel(const int32_t* __restrict__ tables, int32_t mbps
   }
 }
 
+// Host-side checks of a decode / verify call, everything but the workspace.
+// On PA_OK, *kernel_out is the kernel the call runs (AUTO resolved).
+pa_status attend_check(const pa_cache* cache, const void* q, const void* out, const void* k_new,
+                       const void* v_new, const int32_t* slots, int32_t nq, const int32_t* tables,
+                       int32_t mbps, const int32_t* lens, int32_t batch, int32_t q_heads, int32_t max_ctx,
+                       float scale, const pa_options* opts, int32_t* kernel_out) {
+  pa_status st = check_cache(cache);
+  if (st != PA_OK) return st;
+  if (batch < 0 || max_ctx < 0 || nq < 1 || q_heads <= 0) return PA_ERR_INVALID_ARG;
+  if (q_heads % cache->kv_heads) return PA_ERR_INVALID_ARG;
+  if (!std::isfinite(scale)) return PA_ERR_INVALID_ARG;
+  const int32_t split = split_of(opts);
+  if (split % kBlockSize || split > kMaxSplitTokens) return PA_ERR_UNSUPPORTED;
+  int32_t kernel = opts ? opts->kernel : PA_KERNEL_AUTO;
+  if (kernel != PA_KERNEL_AUTO && kernel != PA_KERNEL_MMA && kernel != PA_KERNEL_SIMT) return PA_ERR_UNSUPPORTED;
+  const bool int8 = cache->dtype == PA_DTYPE_INT8;
+  if (int8 && kernel == PA_KERNEL_SIMT) return PA_ERR_UNSUPPORTED;
+  const bool bf16 = cache->dtype == PA_DTYPE_BF16 || int8;  // int8: q / out / new rows are bf16
+  if (kernel == PA_KERNEL_AUTO) kernel = bf16 ? PA_KERNEL_MMA : PA_KERNEL_SIMT;
+  if (kernel == PA_KERNEL_MMA && !bf16) return PA_ERR_UNSUPPORTED;
+  *kernel_out = kernel;
+  if (batch == 0) return PA_OK;
+  if (!q || !out || !tables || !lens || !aligned16(q) || !aligned16(out)) return PA_ERR_INVALID_ARG;
+  if (mbps <= 0 || int64_t(max_ctx) > int64_t(mbps) * kBlockSize) return PA_ERR_INVALID_ARG;
+  const bool fused = (k_new != nullptr);
+  if (fused && (!v_new || !slots || !aligned16(k_new) || !aligned16(v_new))) return PA_ERR_INVALID_ARG;
+  return PA_OK;
+}
+
 // Shared by pa_decode and pa_verify.
 // query_start: null for num_queries (nq) tokens per sequence; otherwise the
 // ragged layout ([batch + 1] offsets into total_queries tokens, at most nq per
@@ -268,31 +300,15 @@ pa_status attend(const pa_cache* cache, const void* q, void* out, const void* k_
                  int32_t mbps, const int32_t* lens, int32_t batch, int32_t q_heads,
                  int32_t max_ctx, float scale, void* ws, size_t ws_bytes, const pa_options* opts,
                  void* stream_ptr, const int32_t* query_start = nullptr, int32_t total_queries = 0) {
-  pa_status st = check_cache(cache);
-  if (st != PA_OK) return st;
-  if (batch < 0 || max_ctx < 0 || nq < 1 || q_heads <= 0) return PA_ERR_INVALID_ARG;
-  if (q_heads % cache->kv_heads) return PA_ERR_INVALID_ARG;
-  if (!std::isfinite(scale)) return PA_ERR_INVALID_ARG;
+  int32_t kernel = PA_KERNEL_AUTO;
+  const pa_status st = attend_check(cache, q, out, k_new, v_new, slots, nq, tables, mbps, lens, batch, q_heads,
+                                    max_ctx, scale, opts, &kernel);
+  if (st != PA_OK || batch == 0) return st;
   const int32_t split = split_of(opts);
-  if (split % kBlockSize || split > kMaxSplitTokens) return PA_ERR_UNSUPPORTED;
-  int32_t kernel = opts ? opts->kernel : PA_KERNEL_AUTO;
-  if (kernel < PA_KERNEL_AUTO || kernel > PA_KERNEL_MMA_LDG) return PA_ERR_UNSUPPORTED;
   const bool int8 = cache->dtype == PA_DTYPE_INT8;
-  if (int8 && kernel != PA_KERNEL_AUTO && kernel != PA_KERNEL_MMA) return PA_ERR_UNSUPPORTED;
-  const bool bf16 = cache->dtype == PA_DTYPE_BF16 || int8;  // int8: q / out / new rows are bf16
-  if (kernel == PA_KERNEL_AUTO) kernel = bf16 ? PA_KERNEL_MMA : PA_KERNEL_SIMT;
-  const bool use_mma = kernel == PA_KERNEL_MMA || kernel == PA_KERNEL_MMA_LDG;
-  if (use_mma && !bf16) return PA_ERR_UNSUPPORTED;
-  if (query_start && kernel == PA_KERNEL_MMA_LDG) return PA_ERR_UNSUPPORTED;
-  const int32_t prefetch = (opts && opts->prefetch > 0) ? opts->prefetch : PA_DEFAULT_PREFETCH;
-  if (prefetch > 2) return PA_ERR_UNSUPPORTED;
-  const int32_t warps = (opts && opts->warps > 0) ? opts->warps : PA_DEFAULT_WARPS;
-  if (warps != 1 && warps != 2 && warps != 4) return PA_ERR_UNSUPPORTED;
-  if (batch == 0) return PA_OK;
-  if (!q || !out || !tables || !lens || !aligned16(q) || !aligned16(out)) return PA_ERR_INVALID_ARG;
-  if (mbps <= 0 || int64_t(max_ctx) > int64_t(mbps) * kBlockSize) return PA_ERR_INVALID_ARG;
+  const bool bf16 = cache->dtype == PA_DTYPE_BF16 || int8;
+  const bool use_mma = kernel == PA_KERNEL_MMA;
   const bool fused = (k_new != nullptr);
-  if (fused && (!v_new || !slots || !aligned16(k_new) || !aligned16(v_new))) return PA_ERR_INVALID_ARG;
 
   WsLayout L;
   const int32_t split_long = split_long_of(opts, cache->dtype);
@@ -341,9 +357,10 @@ pa_status attend(const pa_cache* cache, const void* q, void* out, const void* k_
   // leave the merge to merge_kernel.
   p.merge_in_kernel = kernel == PA_KERNEL_SIMT ? 1 : 0;
   p.scale_log2 = scale * 1.4426950408889634f;
+  p.wait_limit_ns = wait_limit_of(opts);
 
   const int64_t gz = int64_t(batch) * p.row_groups;
-  if (kernel != PA_KERNEL_MMA_LDG && gz > 65535) return PA_ERR_UNSUPPORTED;
+  if (gz > 65535) return PA_ERR_UNSUPPORTED;
   if (int64_t(batch) * cache->kv_heads * p.row_groups * L.max_splits > INT32_MAX) return PA_ERR_UNSUPPORTED;
   const dim3 grid(unsigned(L.max_splits), unsigned(cache->kv_heads), unsigned(gz));
   cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
@@ -364,8 +381,6 @@ pa_status attend(const pa_cache* cache, const void* q, void* out, const void* k_
     if (append_first) e = launch_cache_write_q8(cache, k_new, v_new, slots, p.total_queries, p.status, stream);
     if (e == cudaSuccess) e = launch_attn_q8(maps, p, grid, append_first, stream);
     if (e == cudaSuccess && p.max_splits > 1) e = launch_merge(p, stream);
-  } else if (kernel == PA_KERNEL_MMA_LDG) {
-    e = launch_attn_ldg(p, prefetch, warps, stream);
   } else if (kernel == PA_KERNEL_MMA) {
     CUtensorMap tk, tv;
     if (!make_pool_map(&tk, cache->k, cache->kv_heads, cache->num_blocks) ||
@@ -383,6 +398,16 @@ pa_status attend(const pa_cache* cache, const void* q, void* out, const void* k_
 }  // namespace
 
 namespace pa {
+// pa_decode's host-side checks without the workspace (pa_decode_noalloc runs
+// them before it touches its scratch).
+pa_status decode_check(const pa_cache* cache, const void* q, const void* out, const int32_t* tables, int32_t mbps,
+                       const int32_t* lens, int32_t batch, int32_t q_heads, int32_t max_ctx, float scale,
+                       const pa_options* opts) {
+  int32_t kernel = PA_KERNEL_AUTO;
+  return attend_check(cache, q, out, nullptr, nullptr, nullptr, 1, tables, mbps, lens, batch, q_heads, max_ctx,
+                      scale, opts, &kernel);
+}
+
 // Bytes at the start of a workspace that must be zero when a call starts
 // (status word and arrival counters); 0 if the sizes are invalid.
 size_t workspace_zero_prefix(int32_t batch, int32_t nq, int32_t q_heads, int32_t kv_heads,
@@ -542,6 +567,7 @@ pa_status pa_prefill(const pa_cache* cache, const void* q, void* out, const int3
   p.max_context_len = max_context_len;
   p.split_tokens = kBlockSize;  // unused: a prefill CTA reads its rows' whole visible context
   p.scale_log2 = scale * 1.4426950408889634f;
+  p.wait_limit_ns = wait_limit_of(opts);
   CUtensorMap tk, tv;
   if (!make_pool_map(&tk, cache->k, cache->kv_heads, cache->num_blocks) ||
       !make_pool_map(&tv, cache->v, cache->kv_heads, cache->num_blocks))

@@ -10,6 +10,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <mutex>
+
 #include "../../include/pa.h"
 
 namespace pa {
@@ -20,7 +22,7 @@ constexpr int kRowSlots = 16;         // rows per workspace partial slot (max ro
 constexpr int kMaxSplitTokens = 8192;  // largest split a CTA walks (bounds its block-id buffer)
 constexpr int kConsumerWarps = 4;      // warps that attend; they take blocks round-robin
 constexpr int kCombineStride = kHeadDim + 4;  // padded fp32 row stride of the cross-warp buffer
-constexpr unsigned long long kWaitLimitNs = 1000000000ull;  // bounded waits give up after 1 s
+constexpr uint32_t kWaitLimitNs = PA_DEFAULT_WAIT_LIMIT_NS;  // bounded waits give up after 1 s
 constexpr uint32_t kWaitLimitIters = 1u << 26;
 
 // Everything a CTA needs; passed by value (kernel parameter space).
@@ -55,6 +57,7 @@ struct AttnParams {
   int32_t wait_append;  // int8: 1 if a preceding append grid wrote the new tokens' blocks
   int32_t merge_in_kernel;  // 1: the last split to finish merges; 0: merge_kernel does
   float scale_log2;     // scale * log2(e): scores are kept in base-2 units
+  uint32_t wait_limit_ns;  // bound on the pipeline waits (drains use kWaitLimitNs)
 };
 
 // ---------------------------------------------------------------------------
@@ -99,13 +102,16 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Wait for the phase with the given parity to complete; false after the limit.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+// Wait for the phase with the given parity to complete; false once limit_ns
+// have passed (or after kWaitLimitIters polls). The clock is read every 256
+// polls, or on every poll under a limit below 100 us.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint32_t limit_ns = kWaitLimitNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
+  const uint32_t every = limit_ns < 100000u ? 0u : 255u;
   for (uint32_t it = 1; it < kWaitLimitIters; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 255u) == 0u && global_timer_ns() - t0 > kWaitLimitNs) break;
+    if ((it & every) == 0u && global_timer_ns() - t0 > limit_ns) break;
   }
   return false;
 }
@@ -410,5 +416,24 @@ __device__ void split_epilogue(const AttnParams& p, const CtaWork& w, const floa
   }
   if (threadIdx.x == 0) p.counters[w.unit] = 0;
 }
+
+// ---------------------------------------------------------------------------
+// Host: one-time set-up per device (kernel attributes), safe when several host
+// threads launch at once. run() calls set_up() once for the current device
+// ordinal; later calls return that first result.
+constexpr int kMaxDevices = 64;
+struct PerDeviceOnce {
+  std::once_flag flag[kMaxDevices];
+  cudaError_t result[kMaxDevices] = {};
+  template <typename F>
+  cudaError_t run(F&& set_up) {
+    int dev = 0;
+    const cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    std::call_once(flag[dev], [&] { result[dev] = set_up(dev); });
+    return result[dev];
+  }
+};
 
 }  // namespace pa

@@ -34,7 +34,7 @@ def assert_close(got: np.ndarray, ref: np.ndarray, dtype: str, what: str = ""):
                                f"ref {ref[worst]}, max abs err {np.abs(got - ref).max():.3e}")
 
 
-def gpu_decode(w, kernel="auto", split_tokens=0, write=True, rows=None, prefetch=0, warps=0):
+def gpu_decode(w, kernel="auto", split_tokens=0, write=True, rows=None):
     """Cache write (optional) + pa_decode on the device; returns (out f64, k, v) on the host."""
     import torch
 
@@ -52,15 +52,14 @@ def gpu_decode(w, kernel="auto", split_tokens=0, write=True, rows=None, prefetch
     batch, hq = q.shape[0], q.shape[1]
     ws = pa.new_workspace(batch, 1, hq, w.spec.kv_heads, w.max_context_len, dev, split_tokens)
     out = pa.pa_decode(kc, vc, pa.to_torch(q, dev), pa.to_torch(tables, dev), pa.to_torch(lens, dev),
-                       w.max_context_len, w.scale, ws, split_tokens=split_tokens, kernel=kernel,
-                       prefetch=prefetch, warps=warps)
+                       w.max_context_len, w.scale, ws, split_tokens=split_tokens, kernel=kernel)
     torch.cuda.synchronize()
     status = pa.pa_workspace_status(ws)
     assert status == 0, f"device status flags {status:#x}"
     return pa.to_numpy(out), pa.to_numpy(kc), pa.to_numpy(vc)
 
 
-def gpu_verify(w, kernel="auto", split_tokens=0, warps=0):
+def gpu_verify(w, kernel="auto", split_tokens=0):
     import torch
 
     import paged_kv_decode_pa_gb300 as pa
@@ -72,8 +71,7 @@ def gpu_verify(w, kernel="auto", split_tokens=0, warps=0):
     out = pa.pa_verify(kc, vc, pa.to_torch(w.q, dev), pa.to_torch(w.k_new, dev),
                        pa.to_torch(w.v_new, dev), pa.to_torch(w.slot_mapping, dev),
                        pa.to_torch(w.block_tables, dev), pa.to_torch(w.context_lens, dev),
-                       w.max_context_len, w.scale, ws, split_tokens=split_tokens, kernel=kernel,
-                       warps=warps)
+                       w.max_context_len, w.scale, ws, split_tokens=split_tokens, kernel=kernel)
     torch.cuda.synchronize()
     status = pa.pa_workspace_status(ws)
     assert status == 0, f"device status flags {status:#x}"

@@ -26,6 +26,17 @@ def declared_functions():
     return sorted(set(re.findall(r"^[a-z_ *]*?\b(pa_[a-z_]+)\s*\(", text, flags=re.M)))
 
 
+def test_options_layout_matches_header():
+    """pa_options as the header declares it: the binding's struct has the same
+    fields in the same order and size."""
+    text = HEADER.read_text()
+    body = re.search(r"typedef struct pa_options \{(.*?)\} pa_options;", text, flags=re.S).group(1)
+    body = re.sub(r"/\*.*?\*/", " ", body, flags=re.S)
+    fields = re.findall(r"(int32_t|uint32_t)\s+(\w+);", body)
+    ctypes_of = {"int32_t": ctypes.c_int32, "uint32_t": ctypes.c_uint32}
+    assert [(n, ctypes_of[t]) for t, n in fields] == list(_lib.PaOptions._fields_)
+
+
 def test_header_declares_the_binding_list():
     assert declared_functions() == sorted(_lib.EXPORTED)
 
@@ -38,7 +49,7 @@ def test_every_declared_symbol_is_exported(lib):
 def test_header_constants_match_binding():
     text = HEADER.read_text()
     for name in ("PA_FLAG_BAD_BLOCK", "PA_FLAG_BAD_LENGTH", "PA_FLAG_BAD_SLOT", "PA_FLAG_TIMEOUT",
-                 "PA_DEFAULT_SPLIT_TOKENS", "PA_VALIDATE_WORDS", "PA_DEFAULT_PREFETCH",
+                 "PA_DEFAULT_SPLIT_TOKENS", "PA_VALIDATE_WORDS", "PA_DEFAULT_WAIT_LIMIT_NS",
                  "PA_LONG_CONTEXT_TOKENS", "PA_DEFAULT_SPLIT_LONG", "PA_DEFAULT_SPLIT_LONG_INT8"):
         m = re.search(rf"#define {name} (0x[0-9a-f]+|\d+)", text)
         assert m and int(m.group(1), 0) == getattr(_lib, name), name
@@ -84,8 +95,8 @@ def test_bad_call_arguments_rejected(lib):
     assert _decode(lib, c, opts=_lib.PaOptions(0, 9)) == _lib.PA_ERR_UNSUPPORTED
     f32 = _cache(dtype=_lib.PA_DTYPE_F32)
     assert _decode(lib, f32, opts=_lib.PaOptions(0, _lib.PA_KERNEL_MMA)) == _lib.PA_ERR_UNSUPPORTED
-    assert _decode(lib, f32, opts=_lib.PaOptions(0, _lib.PA_KERNEL_MMA_LDG)) == _lib.PA_ERR_UNSUPPORTED
-    assert _decode(lib, c, opts=_lib.PaOptions(0, 0, 3)) == _lib.PA_ERR_UNSUPPORTED   # prefetch > 2
+    assert _decode(lib, c, opts=_lib.PaOptions(0, 3)) == _lib.PA_ERR_UNSUPPORTED    # no kernel 3
+    assert _decode(lib, c, opts=_lib.PaOptions(0, _lib.PA_KERNEL_TC)) == _lib.PA_ERR_UNSUPPORTED  # prefill only
     assert _decode(lib, c, batch=0) == _lib.PA_OK                      # nothing to do, nothing launched
 
 
@@ -125,7 +136,7 @@ def test_int8_pool_arguments(lib):
     assert _decode(lib, _cache(**ok), batch=0) == _lib.PA_OK
     assert _decode(lib, _cache(**{**ok, "k_scale": None})) == _lib.PA_ERR_INVALID_ARG
     assert _decode(lib, _cache(**{**ok, "v_scale": 0x120004})) == _lib.PA_ERR_INVALID_ARG
-    for kernel in (_lib.PA_KERNEL_SIMT, _lib.PA_KERNEL_MMA_LDG):
+    for kernel in (_lib.PA_KERNEL_SIMT, 3):
         assert _decode(lib, _cache(**ok), opts=_lib.PaOptions(0, kernel)) == _lib.PA_ERR_UNSUPPORTED
     assert lib.pa_cache_write(ctypes.byref(_cache(**{**ok, "k_scale": None})), 0x80000, 0x90000, 0xa0000, 4,
                               None) == _lib.PA_ERR_INVALID_ARG
@@ -142,7 +153,7 @@ def test_prefill_arguments(lib):
     text = HEADER.read_text()
     assert re.search(r"PA_KERNEL_TC = (\d+)", text).group(1) == str(_lib.PA_KERNEL_TC)
     c = _cache()
-    for kernel in (_lib.PA_KERNEL_SIMT, _lib.PA_KERNEL_MMA_LDG, 9):
+    for kernel in (_lib.PA_KERNEL_SIMT, 3, 9):
         assert _prefill(lib, c, _lib.PaOptions(0, kernel)) == _lib.PA_ERR_UNSUPPORTED
     for kernel in (_lib.PA_KERNEL_AUTO, _lib.PA_KERNEL_TC, _lib.PA_KERNEL_MMA):
         assert _prefill(lib, c, _lib.PaOptions(0, kernel), batch=0) == _lib.PA_OK
@@ -157,3 +168,19 @@ def test_prefill_tc_needs_group_of_at_most_128(lib):
     """The tcgen05 prefill kernel takes whole tokens per 128-row tile."""
     c = _cache()
     assert _prefill(lib, c, _lib.PaOptions(0, _lib.PA_KERNEL_TC), hq=2 * 129) == _lib.PA_ERR_UNSUPPORTED
+
+
+def test_noalloc_checks_arguments_like_pa_decode_first(lib):
+    """pa_decode_noalloc returns pa_decode's status for a bad argument even
+    when the sizes would also exceed its scratch: the checks run before the
+    scratch is sized or touched (nothing here reaches the GPU)."""
+    def noalloc(cache, batch=4096, max_ctx=1 << 16, hq=12, opts=None):
+        return lib.pa_decode_noalloc(ctypes.byref(cache), 0x30000, 0x40000, 0x50000, max_ctx // 16, 0x60000, batch,
+                                     hq, max_ctx, ctypes.c_float(0.1), ctypes.byref(opts) if opts else None, None)
+    big = dict(batch=4096, max_ctx=1 << 16)
+    assert noalloc(_cache(head_dim=64), **big) == _lib.PA_ERR_UNSUPPORTED
+    assert noalloc(_cache(), opts=_lib.PaOptions(24, 0), **big) == _lib.PA_ERR_UNSUPPORTED
+    assert noalloc(_cache(), opts=_lib.PaOptions(0, 9), **big) == _lib.PA_ERR_UNSUPPORTED
+    assert noalloc(_cache(), hq=13, **big) == _lib.PA_ERR_INVALID_ARG
+    assert noalloc(_cache(), **big) == _lib.PA_ERR_WORKSPACE
+    assert noalloc(_cache(), batch=0, max_ctx=64) == _lib.PA_OK

@@ -20,7 +20,7 @@ from paged_kv_decode_pa_gb300 import inputs
 pytestmark = pytest.mark.gpu
 
 
-@pytest.mark.parametrize("kernel", ["mma", "mma_ldg", "simt"])
+@pytest.mark.parametrize("kernel", ["mma", "simt"])
 def test_block_relabelling_is_bit_identical(kernel):
     w = inputs.custom(batch=5, q_heads=12, kv_heads=2, context_lens=(3, 40, 333, 600, 1100),
                       num_blocks=200, dtype="bf16", seed=17)
@@ -63,8 +63,7 @@ def test_padded_rows_touch_only_the_spare_block():
     assert_close(to_f64(full[:57]), ref, "bf16", "c3 padded, real rows")
 
 
-@pytest.mark.parametrize("dtype,kernel", [("bf16", "mma"), ("bf16", "mma_ldg"), ("bf16", "simt"),
-                                          ("f32", "simt")])
+@pytest.mark.parametrize("dtype,kernel", [("bf16", "mma"), ("bf16", "simt"), ("f32", "simt")])
 def test_single_token_returns_v_exactly(dtype, kernel):
     w = inputs.custom(batch=4, q_heads=16, kv_heads=8, context_lens=(1, 1, 1, 1), num_blocks=8,
                       dtype=dtype, seed=23)

@@ -48,7 +48,7 @@ def test_validate_counts_bad_entries():
     assert flags == _lib.PA_FLAG_BAD_LENGTH | _lib.PA_FLAG_BAD_BLOCK | _lib.PA_FLAG_BAD_SLOT
 
 
-@pytest.mark.parametrize("kernel", ["mma", "mma_ldg", "simt"])
+@pytest.mark.parametrize("kernel", ["mma", "simt"])
 def test_decode_flags_bad_ids_and_reads_nothing_outside(kernel):
     import torch
 

@@ -9,7 +9,7 @@ from paged_kv_decode_pa_gb300 import inputs
 pytestmark = pytest.mark.gpu
 
 
-@pytest.mark.parametrize("kernel", ["auto", "mma_ldg", "simt"])
+@pytest.mark.parametrize("kernel", ["auto", "simt"])
 def test_verify_c5_matches_oracle(kernel):
     w = workload("c5")
     ref, okc, ovc = oracle_verify_of(w)
@@ -29,8 +29,8 @@ def test_verify_shapes(nq, hq, hkv, split):
     if nq == 1:
         w.q = w.q[:, None]
     ref, okc, ovc = oracle_verify_of(w)
-    for kernel, warps in (("auto", 0), ("mma_ldg", 1), ("mma_ldg", 0)):
-        out, gk, gv = gpu_verify(w, split_tokens=split, kernel=kernel, warps=warps)
+    for kernel in ("auto", "simt"):
+        out, gk, gv = gpu_verify(w, split_tokens=split, kernel=kernel)
         assert gk.tobytes() == okc.tobytes() and gv.tobytes() == ovc.tobytes()
         assert_close(to_f64(out), ref, "bf16", f"verify nq={nq} {hq}/{hkv} {kernel} split {split}")
 
@@ -63,7 +63,7 @@ def _with_negative_slots(w, which):
     return w
 
 
-@pytest.mark.parametrize("kernel", ["auto", "mma_ldg", "simt"])
+@pytest.mark.parametrize("kernel", ["auto", "simt"])
 @pytest.mark.parametrize("hq,hkv", [(16, 8), (32, 4)])
 def test_verify_negative_slots(kernel, hq, hkv):
     """A new token with a negative slot is not written, and attention sees the
@@ -80,7 +80,7 @@ def test_verify_negative_slots(kernel, hq, hkv):
     assert_close(to_f64(out), ref, "bf16", f"negative slots {hq}/{hkv} {kernel}")
 
 
-@pytest.mark.parametrize("kernel", ["auto", "mma_ldg", "simt"])
+@pytest.mark.parametrize("kernel", ["auto", "simt"])
 @pytest.mark.parametrize("split", [0, 48])
 def test_verify_many_new_tokens(kernel, split):
     """100 new tokens per sequence, one query head per KV head: seven row

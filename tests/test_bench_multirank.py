@@ -69,9 +69,14 @@ def test_two_gloo_ranks(tmp_path):
 
 
 def test_rank0_replica_is_the_single_gpu_workload():
+    """Rank 0 times the single-GPU workload: for the 64-request decode, its
+    bucket of 57 sequences and 7 padded rows on the spare block."""
     a = bench.rank_workload("c3", 0)
-    b = bench.inputs.make("c3")
+    b = bench.inputs.make("c3", padded_rows=7)
     assert np.array_equal(a.context_lens, b.context_lens) and np.array_equal(a.block_tables, b.block_tables)
+    assert a.real_rows == 57 and np.all(a.block_tables[57:] == a.spare_block)
+    c = bench.rank_workload("c4", 0)
+    assert np.array_equal(c.block_tables, bench.inputs.make("c4").block_tables)
 
 
 def test_whole_job_rate():

@@ -163,8 +163,10 @@ def test_prefill_large_groups(hq, kernel):
 
 _LONG = dict(batch=8, q_heads=12, kv_heads=2, context_lens=(4096,) * 8, num_blocks=2100, seed=61, num_queries=2048)
 # Sampled rows of the long workload: (sequence, first row of its chunk, rows).
-# The chunk's first rows see the shortest contexts, its last rows the longest.
-_LONG_SAMPLES = ((0, 0, 256), (7, 1536, 512))
+# The chunk's first rows see the shortest contexts, its last rows the longest;
+# the middle samples cross several row tiles (21 tokens each for a group of 6)
+# and so the persistent grid's item boundaries.
+_LONG_SAMPLES = ((0, 0, 256), (3, 1000, 100), (5, 1337, 64), (7, 1536, 512))
 
 
 @functools.lru_cache(maxsize=1)
@@ -187,7 +189,8 @@ def _long_reference():
 def test_prefill_long_chunks_full_size(kernel):
     """The benchmark's long workload at full size (8 sequences, 2048-token
     chunks after 2048-token prefixes, 12/2 heads), in the benchmark's launch
-    configuration; the oracle checks sampled rows of two sequences."""
+    configuration; the oracle checks sampled rows of four sequences, at the
+    start, in the middle and at the end of their chunks."""
     import torch
 
     import paged_kv_decode_pa_gb300 as pa

@@ -13,13 +13,17 @@
 // Attention step. The bytes stay exact in f16: a byte c placed as the low
 // mantissa byte of the f16 pattern 0x64cc is 1024 + c, and subtracting 1152
 // leaves c - 128 with no rounding. Scores are a sum over channels of
-// K code x (K scale x q), so K's per-channel scales multiply the query
-// fragments once per block (f16, 11-bit mantissa); V's per-row scales fold
-// into the softmax weights (P' = p * s_row, one f16 rounding: 2^-12 of the
-// weight, well inside the output tolerance). Both products run on m16n8k16
-// f16 tensor-core MMAs with fp32 accumulation. The accumulator is rescaled
-// only when some row's running maximum grew in the block (otherwise the
-// factor is exactly 1).
+// K code x (K scale x q), so K's per-channel scales multiply the query once
+// per block, in fp32, and the product enters the MMA as two f16 parts (hi +
+// lo, about 22 bits): a single f16 rounding (2^-11 of each term) would put
+// an error of that relative size on every score, which the exponential turns
+// into percent-level weight errors once scores are large (sharply peaked
+// rows). V's per-row scales fold into the softmax weights (P' = p * s_row,
+// one f16 rounding: 2^-12 of the weight, well inside the output tolerance).
+// Both products run on m16n8k16 f16 tensor-core MMAs with fp32
+// accumulation. The accumulator is rescaled only when some row's running
+// maximum grew in the block (otherwise the factor is exactly 1). A product
+// q x (K scale) beyond the f16 range (|x| > 65504) is not supported.
 //
 // Fragments straight from the byte tiles. ldmatrix of a 16-row x 128-byte
 // tile in 16-bit units gives each lane 4 consecutive bytes of a row. A dot
@@ -87,17 +91,33 @@ constexpr uint32_t kSelB23 = 0x5342u;  // bytes 2, 3
 constexpr uint32_t kSelB02 = 0x5240u;  // bytes 0, 2
 constexpr uint32_t kSelB13 = 0x5341u;  // bytes 1, 3
 
-__device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b) {
-  uint32_t r;
-  asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
-  return r;
-}
-
 // Pack two fp32 into f16x2 (round to nearest even): lo in bits 0..15.
 __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
   uint32_t r;
   asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
   return r;
+}
+
+// The two f16 halves of x as fp32 (exact).
+__device__ __forceinline__ void unpack_f16x2(uint32_t x, float& lo, float& hi) {
+  asm("{\n\t.reg .f16 a, b;\n\t"
+      "mov.b32 {a, b}, %2;\n\t"
+      "cvt.f32.f16 %0, a;\n\t"
+      "cvt.f32.f16 %1, b;\n\t}"
+      : "=f"(lo), "=f"(hi)
+      : "r"(x));
+}
+
+// Four fp32 products as two f16x2 pairs each: hi = f16(p), lo = f16(p - hi).
+__device__ __forceinline__ void split_f16(float p0, float p1, float p2, float p3, uint32_t& h01, uint32_t& h23,
+                                          uint32_t& l01, uint32_t& l23) {
+  h01 = pack_f16x2(p0, p1);
+  h23 = pack_f16x2(p2, p3);
+  float a0, a1, a2, a3;
+  unpack_f16x2(h01, a0, a1);
+  unpack_f16x2(h23, a2, a3);
+  l01 = pack_f16x2(p0 - a0, p1 - a1);
+  l23 = pack_f16x2(p2 - a2, p3 - a3);
 }
 
 // D (16x8 fp32) += A (16x16 f16, row) * B (16x8 f16, col)
@@ -110,9 +130,9 @@ __device__ __forceinline__ void mma_f16_16816(float (&d)[4], const uint32_t (&a)
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
-// Q^T as f16 B fragments in the permuted k order: qb[kk][nt][0] = dims
-// 16kk + 4c, +1 of row nt*8 + g; [1] = dims 16kk + 4c + 2, +3. Rows past the
-// group are zero.
+// Q^T in the permuted k order, as the query's own bf16 pairs: qb[kk][nt][0]
+// = dims 16kk + 4c, +1 of row nt*8 + g; [1] = dims 16kk + 4c + 2, +3. Rows
+// past the group are zero. Each block multiplies them by its K scales.
 template <int NT>
 __device__ __forceinline__ void q8_load_q(const uint16_t* q_rows, const int64_t (&row_off)[NT],
                                           const bool (&live)[NT], int c, uint32_t (&qb)[8][NT][2]) {
@@ -122,8 +142,8 @@ __device__ __forceinline__ void q8_load_q(const uint16_t* q_rows, const int64_t 
     for (int kk = 0; kk < 8; ++kk) {
       uint2 v = make_uint2(0u, 0u);
       if (live[nt]) v = __ldg(reinterpret_cast<const uint2*>(q_rows + row_off[nt] + kk * 16 + 4 * c));
-      qb[kk][nt][0] = pack_f16x2(bf16_lo(v.x), bf16_hi(v.x));
-      qb[kk][nt][1] = pack_f16x2(bf16_lo(v.y), bf16_hi(v.y));
+      qb[kk][nt][0] = v.x;
+      qb[kk][nt][1] = v.y;
     }
 }
 
@@ -157,8 +177,7 @@ __device__ __forceinline__ void attend_blocks_q8(const uint32_t (&stage)[NB], co
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         const int kk = 2 * s + h;
-        const float4 ks = *reinterpret_cast<const float4*>(kst[b] + kk * 16 + 4 * ln.c);
-        const uint32_t s01 = pack_f16x2(ks.x, ks.y), s23 = pack_f16x2(ks.z, ks.w);  // channel scales
+        const float4 ks = *reinterpret_cast<const float4*>(kst[b] + kk * 16 + 4 * ln.c);  // channel scales
         const uint32_t lo = h ? r2 : r0, hi = h ? r3 : r1;
         uint32_t a[4];
         a[0] = q8_pair(lo, kSelB01);
@@ -166,9 +185,14 @@ __device__ __forceinline__ void attend_blocks_q8(const uint32_t (&stage)[NB], co
         a[2] = q8_pair(lo, kSelB23);
         a[3] = q8_pair(hi, kSelB23);
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
-          mma_f16_16816(h ? sc_odd[b][nt] : sc[b][nt], a, hmul2(qb[kk][nt][0], s01),
-                        hmul2(qb[kk][nt][1], s23));
+        for (int nt = 0; nt < NT; ++nt) {
+          const uint32_t qx = qb[kk][nt][0], qy = qb[kk][nt][1];
+          uint32_t h01, h23, l01, l23;
+          split_f16(bf16_lo(qx) * ks.x, bf16_hi(qx) * ks.y, bf16_lo(qy) * ks.z, bf16_hi(qy) * ks.w, h01, h23,
+                    l01, l23);
+          mma_f16_16816(h ? sc_odd[b][nt] : sc[b][nt], a, h01, h23);
+          mma_f16_16816(h ? sc_odd[b][nt] : sc[b][nt], a, l01, l23);
+        }
       }
     }
   }

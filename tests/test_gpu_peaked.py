@@ -1,0 +1,106 @@
+"""Sharply peaked attention against the oracle (GPU).
+
+With the default scale 1/sqrt(128) the scores of N(0, 1) data stay within a
+few units, so a row's running maximum settles early and rarely moves. Large
+scales make each row's weights nearly one-hot and move the maximum by many
+powers of two from block to block and from split to split. That exercises
+the online-softmax rescale of every kernel, the tensor-core prefill's lazy
+reference maximum (O is rescaled only when the maximum grows by more than
+2^8), and the log-sum-exp merge of splits whose partial maxima lie far apart.
+The pages fix the softmax with its maximum subtracted (the stall article's
+Model._layer); the oracle computes it in fp64.
+"""
+
+from __future__ import annotations
+
+import pytest
+
+import oracle
+from gpu_util import assert_close, gpu_decode, gpu_verify, oracle_verify_of, to_f64
+from paged_kv_decode_pa_gb300 import inputs
+
+pytestmark = pytest.mark.gpu
+
+SCALES = [1.0, 4.0]
+LENS = (1, 2, 17, 33, 100, 257, 511, 700, 1025)
+
+
+def _decode_workload(scale, seed, dtype="bf16"):
+    w = inputs.custom(batch=len(LENS), q_heads=12, kv_heads=2, context_lens=LENS, num_blocks=200, dtype=dtype,
+                      seed=seed)
+    w.scale = scale
+    return w
+
+
+@pytest.mark.parametrize("scale", SCALES)
+@pytest.mark.parametrize("kernel,split", [("auto", 0), ("auto", 64), ("simt", 0), ("simt", 64)])
+def test_decode_peaked(scale, kernel, split):
+    w = _decode_workload(scale, seed=int(scale * 10) + split)
+    kc, vc = w.k_cache.copy(), w.v_cache.copy()
+    oracle.cache_write(kc, vc, w.k_new, w.v_new, w.slot_mapping)
+    ref = oracle.decode(kc, vc, w.q, w.block_tables, w.context_lens, w.scale)
+    out, _, _ = gpu_decode(w, kernel=kernel, split_tokens=split)
+    assert_close(to_f64(out), ref, "bf16", f"peaked decode scale {scale} {kernel} split {split}")
+
+
+@pytest.mark.parametrize("scale", SCALES)
+@pytest.mark.parametrize("split", [0, 48])
+def test_verify_peaked(scale, split):
+    """Four new tokens per sequence, 16/8 heads (one row group) and 32/4 (two)."""
+    for hq, hkv in ((16, 8), (32, 4)):
+        w = inputs.custom(batch=len(LENS), q_heads=hq, kv_heads=hkv, context_lens=tuple(max(4, x) for x in LENS),
+                          num_blocks=200, dtype="bf16", seed=hq + int(scale), num_queries=4)
+        w.scale = scale
+        ref, okc, ovc = oracle_verify_of(w)
+        out, gk, gv = gpu_verify(w, split_tokens=split)
+        assert gk.tobytes() == okc.tobytes() and gv.tobytes() == ovc.tobytes()
+        assert_close(to_f64(out), ref, "bf16", f"peaked verify {hq}/{hkv} scale {scale} split {split}")
+
+
+@pytest.mark.parametrize("scale", SCALES)
+def test_int8_decode_peaked(scale):
+    import torch
+
+    import paged_kv_decode_pa_gb300 as pa
+
+    w = _decode_workload(scale, seed=70 + int(scale))
+    pool = inputs.q8_pool(w)
+    dev = torch.device("cuda")
+    kq, vq, ks, vs = (pa.to_torch(a, dev) for a in (pool.k_codes, pool.v_codes, pool.k_scale, pool.v_scale))
+    ws = pa.new_workspace(w.spec.batch, 1, w.spec.q_heads, w.spec.kv_heads, w.max_context_len, dev)
+    out = pa.pa_decode(kq, vq, pa.to_torch(w.q, dev), pa.to_torch(w.block_tables, dev),
+                       pa.to_torch(w.context_lens, dev), w.max_context_len, w.scale, ws, k_scale=ks, v_scale=vs)
+    torch.cuda.synchronize()
+    assert pa.pa_workspace_status(ws) == 0
+    ref = oracle.decode_q8(pool.k_codes, pool.v_codes, pool.k_scale, pool.v_scale, w.q, w.block_tables,
+                           w.context_lens, w.scale)
+    assert_close(to_f64(pa.to_numpy(out)), ref, "bf16", f"peaked int8 decode scale {scale}")
+
+
+@pytest.mark.parametrize("scale", SCALES)
+@pytest.mark.parametrize("kernel", ["tc", "mma"])
+def test_prefill_peaked(scale, kernel):
+    """Chunks after prefixes: the causal rows' maxima climb as positions are
+    added, so the lazy reference maximum of the tensor-core kernel moves
+    (and O is rescaled) many times within a row tile."""
+    import torch
+
+    import paged_kv_decode_pa_gb300 as pa
+
+    prefixes, chunks = (0, 100, 700, 31), (200, 129, 300, 64)
+    lens = tuple(p + c for p, c in zip(prefixes, chunks))
+    w = inputs.custom(batch=len(lens), q_heads=16, kv_heads=8, context_lens=lens, num_blocks=200, seed=90,
+                      num_queries=max(chunks))
+    w.scale = scale
+    rw = inputs.ragged(w, list(chunks))
+    dev = torch.device("cuda")
+    kc, vc = pa.to_torch(w.k_cache, dev), pa.to_torch(w.v_cache, dev)
+    ws = torch.zeros(256, dtype=torch.uint8, device=dev)
+    out = pa.pa_prefill(kc, vc, pa.to_torch(rw.q, dev), pa.to_torch(rw.query_start, dev),
+                        pa.to_torch(w.block_tables, dev), pa.to_torch(w.context_lens, dev), w.max_context_len,
+                        w.scale, rw.max_queries, workspace=ws, kernel=kernel)
+    torch.cuda.synchronize()
+    assert pa.pa_workspace_status(ws) == 0
+    ref = oracle.attend_ragged(w.k_cache, w.v_cache, rw.q, rw.query_start, w.block_tables, w.context_lens,
+                               w.scale)
+    assert_close(to_f64(pa.to_numpy(out)), ref, "bf16", f"peaked prefill scale {scale} {kernel}")

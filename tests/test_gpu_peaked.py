@@ -104,3 +104,35 @@ def test_prefill_peaked(scale, kernel):
     ref = oracle.attend_ragged(w.k_cache, w.v_cache, rw.q, rw.query_start, w.block_tables, w.context_lens,
                                w.scale)
     assert_close(to_f64(pa.to_numpy(out)), ref, "bf16", f"peaked prefill scale {scale} {kernel}")
+
+
+@pytest.mark.parametrize("scale", SCALES)
+@pytest.mark.parametrize("hq,hkv", [(16, 8), (32, 4)])
+def test_int8_verify_peaked(scale, hq, hkv):
+    """Fused int8 verify (the new tokens' blocks requantised in the kernel for
+    one row group, appended first for two) with sharply peaked rows; the pool
+    stays bit-exact against the oracle's quantised append."""
+    import torch
+
+    import paged_kv_decode_pa_gb300 as pa
+
+    nq = 4
+    lens = tuple(max(nq, x) for x in LENS)
+    w = inputs.custom(batch=len(lens), q_heads=hq, kv_heads=hkv, context_lens=lens, num_blocks=200,
+                      seed=80 + hq + int(scale), num_queries=nq)
+    w.scale = scale
+    pool = inputs.q8_pool(w)
+    ref_pool = [a.copy() for a in (pool.k_codes, pool.v_codes, pool.k_scale, pool.v_scale)]
+    ref = oracle.verify_q8(*ref_pool, w.q, w.k_new, w.v_new, w.slot_mapping, w.block_tables, w.context_lens,
+                           w.scale)
+    dev = torch.device("cuda")
+    kq, vq, ks, vs = (pa.to_torch(a, dev) for a in (pool.k_codes, pool.v_codes, pool.k_scale, pool.v_scale))
+    ws = pa.new_workspace(w.spec.batch, nq, hq, hkv, w.max_context_len, dev)
+    out = pa.pa_verify(kq, vq, pa.to_torch(w.q, dev), pa.to_torch(w.k_new, dev), pa.to_torch(w.v_new, dev),
+                       pa.to_torch(w.slot_mapping, dev), pa.to_torch(w.block_tables, dev),
+                       pa.to_torch(w.context_lens, dev), w.max_context_len, w.scale, ws, k_scale=ks, v_scale=vs)
+    torch.cuda.synchronize()
+    assert pa.pa_workspace_status(ws) == 0
+    for got, want in zip((kq, vq, ks, vs), ref_pool):
+        assert pa.to_numpy(got).tobytes() == want.tobytes()
+    assert_close(to_f64(pa.to_numpy(out)), ref, "bf16", f"peaked int8 verify {hq}/{hkv} scale {scale}")

@@ -72,9 +72,11 @@
  *    rounded to nearest with ties to even. An all-zero group has s = 0 and
  *    bytes 128.
  *  - Queries, new rows and outputs are bf16. Attention dequantises inside
- *    the kernel. K values enter the products rounded to f16; V bytes enter
- *    exactly, with the row scales folded into the softmax weights. K values
- *    must stay below 65504 in magnitude.
+ *    the kernel: the K scales multiply the query in fp32 and each product
+ *    enters the score products as two f16 parts (about 22 bits); V bytes
+ *    enter exactly, with the row scales folded into the softmax weights (one
+ *    f16 rounding of each weight). Each product q * (K scale) must stay below
+ *    65504 in magnitude.
  */
 #ifndef PA_H_
 #define PA_H_

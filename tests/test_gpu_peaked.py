@@ -136,3 +136,41 @@ def test_int8_verify_peaked(scale, hq, hkv):
     for got, want in zip((kq, vq, ks, vs), ref_pool):
         assert pa.to_numpy(got).tobytes() == want.tobytes()
     assert_close(to_f64(pa.to_numpy(out)), ref, "bf16", f"peaked int8 verify {hq}/{hkv} scale {scale}")
+
+
+@pytest.mark.parametrize("kernel", ["auto", "simt"])
+def test_negative_scale(kernel):
+    """Any finite scale is accepted: a negative one ranks the keys the other
+    way round. Masked positions must stay excluded whatever the sign."""
+    w = _decode_workload(-0.5, seed=123)
+    kc, vc = w.k_cache.copy(), w.v_cache.copy()
+    oracle.cache_write(kc, vc, w.k_new, w.v_new, w.slot_mapping)
+    ref = oracle.decode(kc, vc, w.q, w.block_tables, w.context_lens, w.scale)
+    for split in (0, 64):
+        out, _, _ = gpu_decode(w, kernel=kernel, split_tokens=split)
+        assert_close(to_f64(out), ref, "bf16", f"negative scale {kernel} split {split}")
+
+
+@pytest.mark.parametrize("kernel", ["tc", "mma"])
+def test_prefill_negative_scale(kernel):
+    import torch
+
+    import paged_kv_decode_pa_gb300 as pa
+
+    prefixes, chunks = (0, 100, 31), (200, 129, 64)
+    lens = tuple(p + c for p, c in zip(prefixes, chunks))
+    w = inputs.custom(batch=len(lens), q_heads=16, kv_heads=8, context_lens=lens, num_blocks=120, seed=91,
+                      num_queries=max(chunks))
+    w.scale = -0.25
+    rw = inputs.ragged(w, list(chunks))
+    dev = torch.device("cuda")
+    kc, vc = pa.to_torch(w.k_cache, dev), pa.to_torch(w.v_cache, dev)
+    ws = torch.zeros(256, dtype=torch.uint8, device=dev)
+    out = pa.pa_prefill(kc, vc, pa.to_torch(rw.q, dev), pa.to_torch(rw.query_start, dev),
+                        pa.to_torch(w.block_tables, dev), pa.to_torch(w.context_lens, dev), w.max_context_len,
+                        w.scale, rw.max_queries, workspace=ws, kernel=kernel)
+    torch.cuda.synchronize()
+    assert pa.pa_workspace_status(ws) == 0
+    ref = oracle.attend_ragged(w.k_cache, w.v_cache, rw.q, rw.query_start, w.block_tables, w.context_lens,
+                               w.scale)
+    assert_close(to_f64(pa.to_numpy(out)), ref, "bf16", f"negative scale prefill {kernel}")

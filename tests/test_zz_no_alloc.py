@@ -94,6 +94,30 @@ def test_noalloc_python_binding_with_explicit_split():
         assert pa.to_numpy(got).tobytes() == want.tobytes()
 
 
+def test_noalloc_int8_pool_equals_pa_decode():
+    """The int8 pool through the wrapper (its K and V scales passed on), with
+    a 64-token split so that the merge kernel runs: bit-identical to
+    pa_decode with its own workspace."""
+    import torch
+
+    import paged_kv_decode_pa_gb300 as pa
+    from paged_kv_decode_pa_gb300 import inputs
+
+    w = inputs.custom(batch=5, q_heads=16, kv_heads=8, context_lens=(1, 17, 200, 640, 1025), num_blocks=200,
+                      dtype="bf16", seed=404)
+    pool = inputs.q8_pool(w)
+    kq, vq, ks, vs = (pa.to_torch(a) for a in (pool.k_codes, pool.v_codes, pool.k_scale, pool.v_scale))
+    q, tb, ln = pa.to_torch(w.q), pa.to_torch(w.block_tables), pa.to_torch(w.context_lens)
+    s = w.spec
+    ws = pa.new_workspace(s.batch, 1, s.q_heads, s.kv_heads, w.max_context_len, split_tokens=64)
+    want = pa.pa_decode(kq, vq, q, tb, ln, w.max_context_len, w.scale, ws, split_tokens=64, k_scale=ks, v_scale=vs)
+    got = pa.pa_decode_noalloc(kq, vq, q, tb, ln, w.max_context_len, w.scale, split_tokens=64, k_scale=ks,
+                               v_scale=vs)
+    torch.cuda.synchronize()
+    assert pa.pa_workspace_status(ws) == 0
+    assert pa.to_numpy(got).tobytes() == pa.to_numpy(want).tobytes()
+
+
 def test_noalloc_rejects_sizes_beyond_its_scratch():
     import torch
 

@@ -98,26 +98,22 @@ __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
   return r;
 }
 
-// The two f16 halves of x as fp32 (exact).
-__device__ __forceinline__ void unpack_f16x2(uint32_t x, float& lo, float& hi) {
-  asm("{\n\t.reg .f16 a, b;\n\t"
-      "mov.b32 {a, b}, %2;\n\t"
-      "cvt.f32.f16 %0, a;\n\t"
-      "cvt.f32.f16 %1, b;\n\t}"
-      : "=f"(lo), "=f"(hi)
-      : "r"(x));
-}
-
-// Four fp32 products as two f16x2 pairs each: hi = f16(p), lo = f16(p - hi).
-__device__ __forceinline__ void split_f16(float p0, float p1, float p2, float p3, uint32_t& h01, uint32_t& h23,
-                                          uint32_t& l01, uint32_t& l23) {
-  h01 = pack_f16x2(p0, p1);
-  h23 = pack_f16x2(p2, p3);
-  float a0, a1, a2, a3;
-  unpack_f16x2(h01, a0, a1);
-  unpack_f16x2(h23, a2, a3);
-  l01 = pack_f16x2(p0 - a0, p1 - a1);
-  l23 = pack_f16x2(p2 - a2, p3 - a3);
+// q (a bf16 pair) times two fp32 scales as two f16x2 parts, hi + lo: the
+// products in packed fp32, hi = the top 11 significant bits (exact in f16),
+// lo = p - hi exactly, then rounded to f16.
+__device__ __forceinline__ void split_qs(uint32_t q2, float s0, float s1, uint32_t& h, uint32_t& l) {
+  uint64_t p, s, a;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(p) : "f"(bf16_lo(q2)), "f"(bf16_hi(q2)));
+  asm("mov.b64 %0, {%1, %2};" : "=l"(s) : "f"(s0), "f"(s1));
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(p) : "l"(p), "l"(s));
+  a = p & 0xffffe000ffffe000ull;
+  uint64_t d;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(p), "l"(a));
+  float a0, a1, d0, d1;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a0), "=f"(a1) : "l"(a));
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(d0), "=f"(d1) : "l"(d));
+  h = pack_f16x2(a0, a1);
+  l = pack_f16x2(d0, d1);
 }
 
 // D (16x8 fp32) += A (16x16 f16, row) * B (16x8 f16, col)
@@ -186,10 +182,9 @@ __device__ __forceinline__ void attend_blocks_q8(const uint32_t (&stage)[NB], co
         a[3] = q8_pair(hi, kSelB23);
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
-          const uint32_t qx = qb[kk][nt][0], qy = qb[kk][nt][1];
           uint32_t h01, h23, l01, l23;
-          split_f16(bf16_lo(qx) * ks.x, bf16_hi(qx) * ks.y, bf16_lo(qy) * ks.z, bf16_hi(qy) * ks.w, h01, h23,
-                    l01, l23);
+          split_qs(qb[kk][nt][0], ks.x, ks.y, h01, l01);
+          split_qs(qb[kk][nt][1], ks.z, ks.w, h23, l23);
           mma_f16_16816(h ? sc_odd[b][nt] : sc[b][nt], a, h01, h23);
           mma_f16_16816(h ? sc_odd[b][nt] : sc[b][nt], a, l01, l23);
         }

@@ -164,7 +164,7 @@ typedef struct pa_options {
 #define PA_DEFAULT_SPLIT_TOKENS 1536
 #define PA_LONG_CONTEXT_TOKENS 4096
 #define PA_DEFAULT_SPLIT_LONG 1152
-#define PA_DEFAULT_SPLIT_LONG_INT8 768
+#define PA_DEFAULT_SPLIT_LONG_INT8 704
 
 /*
  * pa_cache_write: cache[h, s / 16, s % 16, :] = new[i, h, :] for every token

@@ -35,7 +35,7 @@ PA_FLAG_TIMEOUT = 0x8
 PA_DEFAULT_SPLIT_TOKENS = 1536
 PA_LONG_CONTEXT_TOKENS = 4096
 PA_DEFAULT_SPLIT_LONG = 1152
-PA_DEFAULT_SPLIT_LONG_INT8 = 768
+PA_DEFAULT_SPLIT_LONG_INT8 = 704
 PA_VALIDATE_WORDS = 4
 PA_NOALLOC_SCRATCH_BYTES = 16 << 20
 

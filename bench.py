@@ -629,7 +629,7 @@ def launches_per_step(w, step, split: int, kernel: str, kv: str) -> int:
     elif max_ctx > _lib.PA_LONG_CONTEXT_TOKENS:
         size = _lib.PA_DEFAULT_SPLIT_LONG_INT8 if kv == "int8" else _lib.PA_DEFAULT_SPLIT_LONG
     else:
-        size = _lib.PA_DEFAULT_SPLIT_TOKENS
+        size = _lib.PA_DEFAULT_SPLIT_TOKENS_INT8 if kv == "int8" else _lib.PA_DEFAULT_SPLIT_TOKENS
     splits = max(1, -(-max_ctx // size))
     n = (0 if step.fused else 1) + 1
     tensor_core = kv == "int8" or (kernel in ("auto", "mma") and s.dtype == "bf16")
@@ -822,7 +822,8 @@ def run_native(args):
                 "block_size": s.block_size, "num_blocks": s.num_blocks,
                 "context_tokens": int(w.context_lens.sum()),
                 "split_tokens": args.split_tokens or (
-                    f"default: {_lib.PA_DEFAULT_SPLIT_TOKENS} up to {_lib.PA_LONG_CONTEXT_TOKENS} tokens, "
+                    f"default: {_lib.PA_DEFAULT_SPLIT_TOKENS_INT8 if args.kv == 'int8' else _lib.PA_DEFAULT_SPLIT_TOKENS}"
+                    f" up to {_lib.PA_LONG_CONTEXT_TOKENS} tokens, "
                     f"{_lib.PA_DEFAULT_SPLIT_LONG_INT8 if args.kv == 'int8' else _lib.PA_DEFAULT_SPLIT_LONG} "
                     f"beyond"),
                 "kernel": args.kernel,

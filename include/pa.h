@@ -142,11 +142,14 @@ typedef enum pa_kernel {
 typedef struct pa_options {
     /* Tokens per context split (flash-decoding split-K). A positive multiple
      * of block_size: every sequence uses this split. 0 = the default rule:
-     * PA_DEFAULT_SPLIT_TOKENS for a sequence of up to PA_LONG_CONTEXT_TOKENS
-     * tokens, and PA_DEFAULT_SPLIT_LONG (bf16, fp32) or
-     * PA_DEFAULT_SPLIT_LONG_INT8 (int8 pool) for a longer one. Either way a
-     * sequence's split depends only on its own length, never on its
-     * batch-mates, so its result is bit-identical across batch compositions. */
+     * for a sequence of up to PA_LONG_CONTEXT_TOKENS tokens,
+     * PA_DEFAULT_SPLIT_TOKENS (bf16, fp32) or PA_DEFAULT_SPLIT_TOKENS_INT8
+     * (int8 pool); for a longer one, PA_DEFAULT_SPLIT_LONG (bf16, fp32) or
+     * PA_DEFAULT_SPLIT_LONG_INT8. Either way a sequence's split depends only
+     * on its own length and the pool's format, never on its batch-mates, so
+     * its result is bit-identical across batch compositions. A call whose
+     * longest sequence would need more than 65535 splits returns
+     * PA_ERR_UNSUPPORTED. */
     int32_t split_tokens;
     int32_t kernel;   /* pa_kernel */
     /* Bound, in nanoseconds, on each wait of the tensor-core attention
@@ -161,7 +164,8 @@ typedef struct pa_options {
 
 #define PA_DEFAULT_WAIT_LIMIT_NS 1000000000u
 
-#define PA_DEFAULT_SPLIT_TOKENS 1536
+#define PA_DEFAULT_SPLIT_TOKENS 768
+#define PA_DEFAULT_SPLIT_TOKENS_INT8 1536
 #define PA_LONG_CONTEXT_TOKENS 4096
 #define PA_DEFAULT_SPLIT_LONG 1152
 #define PA_DEFAULT_SPLIT_LONG_INT8 704
@@ -199,7 +203,9 @@ pa_status pa_cache_write(const pa_cache *cache, const void *d_k_new, const void 
  * holds a status word, one arrival counter per (sequence, KV head, row group)
  * and the fp32 split partials. It must be zero-filled once before first use
  * (pa_workspace_init); every call leaves it ready for the next.
- * num_queries is 1 for decode. Returns 0 if an argument is invalid.
+ * num_queries is 1 for decode. Under the default split rule the size covers
+ * either pool format (it counts the finer of their splits). Returns 0 if an
+ * argument is invalid.
  */
 size_t pa_workspace_size(int32_t batch, int32_t num_queries, int32_t q_heads, int32_t kv_heads,
                          int32_t head_dim, int32_t max_context_len, const pa_options *opts);

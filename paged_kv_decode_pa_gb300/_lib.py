@@ -32,7 +32,8 @@ PA_FLAG_BAD_LENGTH = 0x2
 PA_FLAG_BAD_SLOT = 0x4
 PA_FLAG_TIMEOUT = 0x8
 
-PA_DEFAULT_SPLIT_TOKENS = 1536
+PA_DEFAULT_SPLIT_TOKENS = 768
+PA_DEFAULT_SPLIT_TOKENS_INT8 = 1536
 PA_LONG_CONTEXT_TOKENS = 4096
 PA_DEFAULT_SPLIT_LONG = 1152
 PA_DEFAULT_SPLIT_LONG_INT8 = 704

@@ -97,9 +97,9 @@ __global__ void __launch_bounds__(kMmaThreads, NT == 1 ? 4 : 3)
   // length, so the two memory latencies overlap instead of adding up.
   int L_raw;
   {
-    const int b = blockIdx.z / p.row_groups;
+    const int b = blockIdx.y / p.row_groups;
     const int per = p.split_tokens / kBlockSize;
-    const int j0 = blockIdx.x * per;
+    const int j0 = blockIdx.z * per;
     const int jn = min(per, p.mbps - j0);
     L_raw = __ldg(p.context_lens + b);
     for (int j = threadIdx.x; j < jn; j += blockDim.x)
@@ -110,7 +110,7 @@ __global__ void __launch_bounds__(kMmaThreads, NT == 1 ? 4 : 3)
   if (w.split_size != p.split_tokens) {
     // A long sequence with its own split size: its entries start elsewhere.
     // Each thread rewrites the indices it wrote above, so no barrier is needed.
-    const int b = blockIdx.z / p.row_groups;
+    const int b = blockIdx.y / p.row_groups;
     const int j0 = w.t0 / kBlockSize;
     const int jn = min(w.split_size / kBlockSize, p.mbps - j0);
     for (int j = threadIdx.x; j < jn; j += blockDim.x)

@@ -60,8 +60,12 @@ pa_status check_cache(const pa_cache* c) {
   return PA_OK;
 }
 
-int32_t split_of(const pa_options* o) {
-  return (o && o->split_tokens > 0) ? o->split_tokens : PA_DEFAULT_SPLIT_TOKENS;
+// Split for sequences of up to PA_LONG_CONTEXT_TOKENS under the default
+// rule, or the caller's split. Without a dtype (workspace sizing) the finer
+// of the two defaults is taken, an upper bound on splits.
+int32_t split_of(const pa_options* o, int32_t dtype) {
+  if (o && o->split_tokens > 0) return o->split_tokens;
+  return dtype == PA_DTYPE_INT8 ? PA_DEFAULT_SPLIT_TOKENS_INT8 : PA_DEFAULT_SPLIT_TOKENS;
 }
 
 uint32_t wait_limit_of(const pa_options* o) {
@@ -273,7 +277,7 @@ pa_status attend_check(const pa_cache* cache, const void* q, const void* out, co
   if (batch < 0 || max_ctx < 0 || nq < 1 || q_heads <= 0) return PA_ERR_INVALID_ARG;
   if (q_heads % cache->kv_heads) return PA_ERR_INVALID_ARG;
   if (!std::isfinite(scale)) return PA_ERR_INVALID_ARG;
-  const int32_t split = split_of(opts);
+  const int32_t split = split_of(opts, cache->dtype);
   if (split % kBlockSize || split > kMaxSplitTokens) return PA_ERR_UNSUPPORTED;
   int32_t kernel = opts ? opts->kernel : PA_KERNEL_AUTO;
   if (kernel != PA_KERNEL_AUTO && kernel != PA_KERNEL_MMA && kernel != PA_KERNEL_SIMT) return PA_ERR_UNSUPPORTED;
@@ -304,7 +308,7 @@ pa_status attend(const pa_cache* cache, const void* q, void* out, const void* k_
   const pa_status st = attend_check(cache, q, out, k_new, v_new, slots, nq, tables, mbps, lens, batch, q_heads,
                                     max_ctx, scale, opts, &kernel);
   if (st != PA_OK || batch == 0) return st;
-  const int32_t split = split_of(opts);
+  const int32_t split = split_of(opts, cache->dtype);
   const bool int8 = cache->dtype == PA_DTYPE_INT8;
   const bool bf16 = cache->dtype == PA_DTYPE_BF16 || int8;
   const bool use_mma = kernel == PA_KERNEL_MMA;
@@ -360,9 +364,12 @@ pa_status attend(const pa_cache* cache, const void* q, void* out, const void* k_
   p.wait_limit_ns = wait_limit_of(opts);
 
   const int64_t gz = int64_t(batch) * p.row_groups;
-  if (gz > 65535) return PA_ERR_UNSUPPORTED;
+  if (gz > 65535 || L.max_splits > 65535) return PA_ERR_UNSUPPORTED;
   if (int64_t(batch) * cache->kv_heads * p.row_groups * L.max_splits > INT32_MAX) return PA_ERR_UNSUPPORTED;
-  const dim3 grid(unsigned(L.max_splits), unsigned(cache->kv_heads), unsigned(gz));
+  // Splits vary slowest: every (sequence, KV head, row group)'s first split
+  // is scheduled before any second one, so the later splits of the long
+  // sequences fill the slots the short sequences free.
+  const dim3 grid(unsigned(cache->kv_heads), unsigned(gz), unsigned(L.max_splits));
   cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
 
   cudaError_t e;
@@ -450,7 +457,7 @@ size_t pa_workspace_size(int32_t batch, int32_t num_queries, int32_t q_heads, in
                          int32_t head_dim, int32_t max_context_len, const pa_options* opts) {
   if (head_dim != kHeadDim) return 0;
   WsLayout L;
-  if (!ws_layout(batch, num_queries, q_heads, kv_heads, max_context_len, split_of(opts),
+  if (!ws_layout(batch, num_queries, q_heads, kv_heads, max_context_len, split_of(opts, -1),
                  split_long_of(opts, -1), &L))
     return 0;
   return L.total;

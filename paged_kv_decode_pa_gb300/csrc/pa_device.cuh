@@ -257,14 +257,14 @@ __device__ __forceinline__ void seq_queries(const AttnParams& p, int b, bool rep
   query_range(p, __ldg(p.query_start + b), __ldg(p.query_start + b + 1), report, q0, nq);
 }
 
-// The work of CTA (blockIdx.x = split, .y = KV head, .z = sequence x row
-// group); L_raw is context_lens[b] if the caller has loaded it already.
+// The work of CTA (blockIdx.x = KV head, .y = sequence x row group, .z =
+// split); L_raw is context_lens[b] if the caller has loaded it already.
 __device__ __forceinline__ CtaWork cta_work(const AttnParams& p, int L_raw = -2147483647 - 1) {
   CtaWork w;
-  w.split = blockIdx.x;
-  w.h = blockIdx.y;
-  w.b = blockIdx.z / p.row_groups;
-  w.rg = blockIdx.z - w.b * p.row_groups;
+  w.split = blockIdx.z;
+  w.h = blockIdx.x;
+  w.b = blockIdx.y / p.row_groups;
+  w.rg = blockIdx.y - w.b * p.row_groups;
   seq_queries(p, w.b, w.split == 0 && w.h == 0 && w.rg == 0, &w.q0, &w.nq);
   int L = L_raw == -2147483647 - 1 ? __ldg(p.context_lens + w.b) : L_raw;
   const int cap = min(p.max_context_len, p.mbps * kBlockSize);

@@ -67,7 +67,8 @@ extern "C" pa_status pa_decode_noalloc(const pa_cache* cache, const void* q, voi
     pa::record_cuda_error(e);
     return PA_ERR_CUDA;
   }
-  // The previous call's status word and counters must not leak into this one.
+  // The previous call's status word and counters must not leak into this one
+  // (their extent does not depend on the split).
   const int32_t split = (opts && opts->split_tokens > 0) ? opts->split_tokens : PA_DEFAULT_SPLIT_TOKENS;
   const size_t zero = pa::workspace_zero_prefix(batch, 1, q_heads, cache->kv_heads, max_context_len, split);
   e = cudaMemsetAsync(scratch, 0, zero, static_cast<cudaStream_t>(stream));

@@ -50,7 +50,8 @@ def test_header_constants_match_binding():
     text = HEADER.read_text()
     for name in ("PA_FLAG_BAD_BLOCK", "PA_FLAG_BAD_LENGTH", "PA_FLAG_BAD_SLOT", "PA_FLAG_TIMEOUT",
                  "PA_DEFAULT_SPLIT_TOKENS", "PA_VALIDATE_WORDS", "PA_DEFAULT_WAIT_LIMIT_NS",
-                 "PA_LONG_CONTEXT_TOKENS", "PA_DEFAULT_SPLIT_LONG", "PA_DEFAULT_SPLIT_LONG_INT8"):
+                 "PA_LONG_CONTEXT_TOKENS", "PA_DEFAULT_SPLIT_LONG", "PA_DEFAULT_SPLIT_LONG_INT8",
+                 "PA_DEFAULT_SPLIT_TOKENS_INT8"):
         m = re.search(rf"#define {name} (0x[0-9a-f]+|\d+)", text)
         assert m and int(m.group(1), 0) == getattr(_lib, name), name
 

@@ -99,6 +99,10 @@ def test_bad_call_arguments_rejected(lib):
     assert _decode(lib, c, opts=_lib.PaOptions(0, 3)) == _lib.PA_ERR_UNSUPPORTED    # no kernel 3
     assert _decode(lib, c, opts=_lib.PaOptions(0, _lib.PA_KERNEL_TC)) == _lib.PA_ERR_UNSUPPORTED  # prefill only
     assert _decode(lib, c, batch=0) == _lib.PA_OK                      # nothing to do, nothing launched
+    # The split index is the grid's z: more than 65535 splits per sequence is refused before
+    # anything is launched (16-token splits over 65537 blocks).
+    assert _decode(lib, _cache(num_blocks=70000), mbps=65537, max_ctx=16 * 65537, batch=1, hq=2,
+                   ws_bytes=1 << 45, opts=_lib.PaOptions(16, 0)) == _lib.PA_ERR_UNSUPPORTED
 
 
 def test_verify_and_write_arguments(lib):

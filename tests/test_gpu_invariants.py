@@ -47,6 +47,48 @@ def test_batch_invariance():
     assert np.array_equal(full[rows], sub), "a sequence's output changed with its batch-mates"
 
 
+_SPLIT_LENS = (100, 700, 800, 1500, 4096, 4100, 9000, 20)  # across both split thresholds
+
+
+@pytest.mark.parametrize("kernel", ["mma", "simt"])
+def test_batch_invariance_across_split_rules(kernel):
+    """Sequences on either side of the short and long default splits (one
+    split, several, the long-context rule): each one's output is the same bits
+    alone, in a subset, or in the whole batch."""
+    w = inputs.custom(batch=len(_SPLIT_LENS), q_heads=12, kv_heads=2, context_lens=_SPLIT_LENS,
+                      num_blocks=1400, dtype="bf16", seed=29)
+    full, _, _ = gpu_decode(w, kernel=kernel, write=False)
+    for rows in ([6], [2, 5], [0, 3, 7, 1], [4]):
+        sub, _, _ = gpu_decode(w, kernel=kernel, write=False, rows=np.array(rows))
+        assert np.array_equal(full[rows], sub), f"rows {rows}: output changed with the batch-mates"
+
+
+def test_int8_batch_invariance_across_split_rules():
+    import torch
+
+    import paged_kv_decode_pa_gb300 as pa
+
+    w = inputs.custom(batch=len(_SPLIT_LENS), q_heads=12, kv_heads=2, context_lens=_SPLIT_LENS,
+                      num_blocks=1400, dtype="bf16", seed=31)
+    pool = inputs.q8_pool(w)
+    dev = torch.device("cuda")
+    kq, vq, ks, vs = (pa.to_torch(a, dev) for a in (pool.k_codes, pool.v_codes, pool.k_scale, pool.v_scale))
+
+    def run(rows):
+        q = np.ascontiguousarray(w.q[rows])
+        ws = pa.new_workspace(len(rows), 1, 12, 2, w.max_context_len, dev)
+        out = pa.pa_decode(kq, vq, pa.to_torch(q, dev), pa.to_torch(np.ascontiguousarray(w.block_tables[rows]), dev),
+                           pa.to_torch(np.ascontiguousarray(w.context_lens[rows]), dev), w.max_context_len,
+                           w.scale, ws, k_scale=ks, v_scale=vs)
+        torch.cuda.synchronize()
+        assert pa.pa_workspace_status(ws) == 0
+        return pa.to_numpy(out)
+
+    full = run(np.arange(len(_SPLIT_LENS)))
+    for rows in ([6], [2, 5], [0, 3, 7, 1]):
+        assert np.array_equal(full[rows], run(np.array(rows))), f"int8 rows {rows}"
+
+
 def test_padded_rows_touch_only_the_spare_block():
     w = workload("c3", padded_rows=7)
     full, gk, gv = gpu_decode(w)

@@ -9,9 +9,9 @@
 //
 // Warp roles (3 warps):
 //   warp 2      producer: one lane walks the split's block-table entries and
-//               issues TMA tensor loads of each 16-token block, K and V, into a
-//               ring of shared-memory stages (128-byte swizzle, so ldmatrix
-//               reads are bank-conflict free). Each block is a contiguous
+//               issues TMA tensor loads of each 16-token block, one box for
+//               K and one for V, into a ring of shared-memory stages
+//               (128-byte swizzle, so ldmatrix reads are bank-conflict free). Each block is a contiguous
 //               16 x 128 tile of the head-major cache ("2. Head-major KV
 //               cache"): no gather, no padded copy.
 //   warps 0..1  consumers: block j goes to warp j % 2. Per block, a warp
@@ -49,7 +49,7 @@ namespace pa {
 // eight stages, but more CTAs, and so more TMA issuers and a finer grid, per SM.
 constexpr int kMmaConsumers = 2;
 constexpr int kStages = 6;                 // shared-memory ring depth (blocks in flight per CTA)
-constexpr int kStageBytes = kBlockBytes;   // one K+V block; each TMA box is 16 rows x 64 dims
+constexpr int kStageBytes = kBlockBytes;   // one K+V block: one TMA box per tile (16 rows x 2 halves x 64 dims)
 constexpr int kMmaThreads = (kMmaConsumers + 1) * 32;
 
 struct MmaSmem {
@@ -223,10 +223,8 @@ __global__ void __launch_bounds__(kMmaThreads, NT == 1 ? 4 : 3)
       }
       const int y = id >= 0 ? id * kBlockSize : -kBlockSize;
       mbar_arrive_expect_tx(fb, kStageBytes);
-      tma_load_3d(st, &tmap_k, 0, y, w.h, fb, policy);
-      tma_load_3d(st + kHalfTile, &tmap_k, 64, y, w.h, fb, policy);
-      tma_load_3d(st + kTileBytes, &tmap_v, 0, y, w.h, fb, policy);
-      tma_load_3d(st + kTileBytes + kHalfTile, &tmap_v, 64, y, w.h, fb, policy);
+      tma_load_4d(st, &tmap_k, 0, y, 0, w.h, fb, policy);
+      tma_load_4d(st + kTileBytes, &tmap_v, 0, y, 0, w.h, fb, policy);
       return true;
     };
     int issued = 0;

@@ -149,6 +149,22 @@ bool make_pool_map(CUtensorMap* map, void* pool, int32_t kv_heads, int32_t num_b
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// The same pool as a 4-D view [kv_heads][2 halves][num_blocks * 16][64]
+// whose half dimension (128 bytes apart) comes after the rows (256 bytes
+// apart): one box of 64 dims x 16 rows x 2 halves lands a whole 16-row tile
+// as [half][row][64], the layout two 3-D boxes give.
+bool make_pool_map4(CUtensorMap* map, void* pool, int32_t kv_heads, int32_t num_blocks) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[4] = {64, cuuint64_t(num_blocks) * kBlockSize, 2, cuuint64_t(kv_heads)};
+  cuuint64_t strides[3] = {cuuint64_t(kHeadDim) * 2, 128, cuuint64_t(num_blocks) * kBlockSize * kHeadDim * 2};
+  cuuint32_t box[4] = {64, 16, 2, 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, pool, dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // Query rows of a prefill, [total][q_heads][128] bf16, in boxes of 64 dims x
 // `group` heads x `tokens` tokens (128-byte swizzle): a box lands as the rows
 // r = token * group + head of one KV head's group. Outside the tensor it
@@ -390,8 +406,8 @@ pa_status attend(const pa_cache* cache, const void* q, void* out, const void* k_
     if (e == cudaSuccess && p.max_splits > 1) e = launch_merge(p, stream);
   } else if (kernel == PA_KERNEL_MMA) {
     CUtensorMap tk, tv;
-    if (!make_pool_map(&tk, cache->k, cache->kv_heads, cache->num_blocks) ||
-        !make_pool_map(&tv, cache->v, cache->kv_heads, cache->num_blocks))
+    if (!make_pool_map4(&tk, cache->k, cache->kv_heads, cache->num_blocks) ||
+        !make_pool_map4(&tv, cache->v, cache->kv_heads, cache->num_blocks))
       return cuda_fail(cudaErrorInvalidValue);
     e = launch_attn_mma(tk, tv, p, grid, stream);
     if (e == cudaSuccess && p.max_splits > 1) e = launch_merge(p, stream);

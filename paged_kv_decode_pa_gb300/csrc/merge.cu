@@ -73,20 +73,22 @@ __global__ void __launch_bounds__(kMergeWarps * 32) merge_kernel(const AttnParam
   float den = 0.f;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
   if (M != -INFINITY && pre) {
+    // Weights and products are summed in split order, the order the CTA-wide
+    // form combines its warps in: a pair of up to 8 splits gets the same bits
+    // whichever form the launch takes (it depends on the batch's longest
+    // sequence).
     const float wgt = s_first < nsplit ? fast_exp2(first - M) : 0.f;
-    den = wgt;
 #pragma unroll
     for (int k = 0; k < kPre; ++k) {
       if (k < n_w) {
         const float wk = __shfl_sync(0xffffffffu, wgt, k);
+        den += wk;
         acc.x += wk * v[k].x;
         acc.y += wk * v[k].y;
         acc.z += wk * v[k].z;
         acc.w += wk * v[k].w;
       }
     }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) den += __shfl_xor_sync(0xffffffffu, den, off);
   } else if (M != -INFINITY) {
     for (int s0 = part; s0 < nsplit; s0 += kChunk) {
       const int s = s0 + WP * lane;

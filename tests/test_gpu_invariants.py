@@ -89,6 +89,48 @@ def test_int8_batch_invariance_across_split_rules():
         assert np.array_equal(full[rows], run(np.array(rows))), f"int8 rows {rows}"
 
 
+@pytest.mark.parametrize("kv", ["bf16", "int8"])
+def test_batch_invariance_across_merge_forms(kv):
+    """The merge takes a warp per row while the batch's longest sequence has at
+    most 8 splits and a CTA per row beyond; a sequence of a few splits must get
+    the same bits under both."""
+    import torch
+
+    import paged_kv_decode_pa_gb300 as pa
+
+    # 32 sequences of 4 to 8 splits under the long-context rule (and one short one), then a
+    # 32k-token sequence whose 29 splits switch the merge to a CTA per row.
+    rng = np.random.Generator(np.random.PCG64(41))
+    lens = tuple(int(x) for x in rng.integers(4200, 9200, size=32)) + (800, 32768)
+    w = inputs.custom(batch=len(lens), q_heads=12, kv_heads=2, context_lens=lens,
+                      num_blocks=sum(-(-x // 16) for x in lens) + 8, dtype="bf16", seed=37)
+    dev = torch.device("cuda")
+    if kv == "int8":
+        pool = inputs.q8_pool(w)
+        kc, vc, ks, vs = (pa.to_torch(a, dev) for a in (pool.k_codes, pool.v_codes, pool.k_scale, pool.v_scale))
+        scales = {"k_scale": ks, "v_scale": vs}
+    else:
+        kc, vc = pa.to_torch(w.k_cache, dev), pa.to_torch(w.v_cache, dev)
+        scales = {}
+
+    def run(rows):
+        rows = np.array(rows)
+        ws = pa.new_workspace(len(rows), 1, 12, 2, w.max_context_len, dev)
+        out = pa.pa_decode(kc, vc, pa.to_torch(np.ascontiguousarray(w.q[rows]), dev),
+                           pa.to_torch(np.ascontiguousarray(w.block_tables[rows]), dev),
+                           pa.to_torch(np.ascontiguousarray(w.context_lens[rows]), dev), w.max_context_len,
+                           w.scale, ws, **scales)
+        torch.cuda.synchronize()
+        assert pa.pa_workspace_status(ws) == 0
+        return pa.to_numpy(out)
+
+    n = len(lens)
+    full = run(list(range(n)))
+    short = list(range(n - 1))
+    assert np.array_equal(full[short], run(short)), f"{kv}: outputs changed with a 32k-token batch-mate"
+    assert np.array_equal(full[[n - 1]], run([n - 1]))
+
+
 def test_padded_rows_touch_only_the_spare_block():
     w = workload("c3", padded_rows=7)
     full, gk, gv = gpu_decode(w)

@@ -202,7 +202,9 @@ pa_status pa_cache_write(const pa_cache *cache, const void *d_k_new, const void 
  * Bytes of workspace pa_decode / pa_verify need for these sizes. The workspace
  * holds a status word, one arrival counter per (sequence, KV head, row group)
  * and the fp32 split partials. It must be zero-filled once before first use
- * (pa_workspace_init); every call leaves it ready for the next.
+ * (pa_workspace_init); every call leaves it ready for the next, except one
+ * that raised PA_FLAG_TIMEOUT, which may leave arrival counters set: zero-fill
+ * the workspace again before its next use.
  * num_queries is 1 for decode. Under the default split rule the size covers
  * either pool format (it counts the finer of their splits). Returns 0 if an
  * argument is invalid.

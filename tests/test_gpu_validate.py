@@ -8,6 +8,8 @@ slot outside the pool is skipped; a length above the limits is clamped.
 import numpy as np
 import pytest
 
+import oracle
+from gpu_util import assert_close, to_f64
 from paged_kv_decode_pa_gb300 import _lib, inputs
 
 pytestmark = pytest.mark.gpu
@@ -70,3 +72,10 @@ def test_decode_flags_bad_ids_and_reads_nothing_outside(kernel):
     assert pa.pa_workspace_status(ws) == 0
     o, g = pa.to_numpy(out), pa.to_numpy(good)
     assert np.array_equal(o[[0, 2]], g[[0, 2]]), "a bad id in one sequence changed another"
+    # The bad block reads as zeros: the oracle over a pool with one extra all-zero block in its place.
+    kz = np.concatenate([w.k_cache, np.zeros_like(w.k_cache[:, :1])], axis=1)
+    vz = np.concatenate([w.v_cache, np.zeros_like(w.v_cache[:, :1])], axis=1)
+    tz = w.block_tables.copy()
+    tz[1, 1] = w.spec.num_blocks
+    ref = oracle.decode(kz, vz, w.q, tz, w.context_lens, w.scale)
+    assert_close(to_f64(o[[1]]), ref[[1]], "bf16", f"{kernel}: bad block read as zeros")

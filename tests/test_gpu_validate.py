@@ -79,3 +79,33 @@ def test_decode_flags_bad_ids_and_reads_nothing_outside(kernel):
     tz[1, 1] = w.spec.num_blocks
     ref = oracle.decode(kz, vz, w.q, tz, w.context_lens, w.scale)
     assert_close(to_f64(o[[1]]), ref[[1]], "bf16", f"{kernel}: bad block read as zeros")
+
+
+def test_int8_decode_bad_id_reads_a_zero_block():
+    """The int8 pool's tensor loads read zeros (codes and scales) past the pool:
+    the values are those of an all-zero block, and other sequences are untouched."""
+    import torch
+
+    import paged_kv_decode_pa_gb300 as pa
+
+    w = inputs.custom(batch=3, q_heads=12, kv_heads=2, context_lens=(40, 40, 40), num_blocks=16,
+                      dtype="bf16", seed=47)
+    pool = inputs.q8_pool(w)
+    kq, vq, ks, vs = (pa.to_torch(a) for a in (pool.k_codes, pool.v_codes, pool.k_scale, pool.v_scale))
+    tables = w.block_tables.copy()
+    tables[1, 1] = 1 << 30
+    ws = pa.new_workspace(3, 1, 12, 2, 40)
+    out = pa.pa_decode(kq, vq, pa.to_torch(w.q), pa.to_torch(tables), pa.to_torch(w.context_lens), 40, w.scale, ws,
+                       k_scale=ks, v_scale=vs)
+    torch.cuda.synchronize()
+    assert pa.pa_workspace_status(ws) & _lib.PA_FLAG_BAD_BLOCK
+    o = pa.to_numpy(out)
+
+    def extend(a, fill):
+        return np.concatenate([a, np.full_like(a[:, :1], fill)], axis=1)
+
+    tz = w.block_tables.copy()
+    tz[1, 1] = w.spec.num_blocks
+    ref = oracle.decode_q8(extend(pool.k_codes, 128), extend(pool.v_codes, 128), extend(pool.k_scale, 0),
+                           extend(pool.v_scale, 0), w.q, tz, w.context_lens, w.scale)
+    assert_close(to_f64(o), ref, "bf16", "int8: bad block read as zeros")
